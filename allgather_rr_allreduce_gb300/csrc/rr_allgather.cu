@@ -1,0 +1,307 @@
+// Rank-major and param-contiguous allgather over W ranks emulated on one GPU.
+//
+// Rank-major all_gather_into_tensor is the param-contiguous gather with a
+// single split, so one kernel serves both.  Rank r's shard is a run of params:
+// bytes [off[s], off[s+1]) of the shard hold its piece of param s, and that
+// piece lands at byte off[s]*W + r*(off[s+1]-off[s]) of every materialised
+// output ("ccl: hierarchical cross-node AllGather (intra-node SDMA +
+// inter-node RDMA) #441": rank r lands at O_s*W + r*E_s; one fused launch over
+// every (rank, param) slot).
+//
+// Each rank pushes its own shard into the outputs, as that PR's direct
+// scatter does: block (r, b) reads region b of shard r once and writes it to
+// every output, so a byte is read from HBM once however many outputs exist.
+// Barriers: ARRIVE (every rank has entered, so its output may be written),
+// END on block b (every push of region b has landed before anyone leaves).
+//
+// Two engines:
+//   ldst: 256 threads move 16-byte vectors (8-byte / 4-byte / 2-byte words
+//         when a piece is not 16-byte aligned).
+//   tma:  one thread of the block drives a ring of shared-memory stages with
+//         cp.async.bulk (global -> shared, completion on an mbarrier) and
+//         cp.async.bulk (shared -> global, bulk groups), one load feeding one
+//         store per output; the other warps copy the pieces the bulk engine
+//         cannot take (not 16-byte aligned, or the last < 16 bytes).
+#include "rr_device.cuh"
+
+namespace rr {
+
+constexpr int kLdstThreads = 256;
+constexpr int kTmaThreads = 128;
+constexpr int kTmaStages = 4;
+constexpr int kTmaChunk = 16384;  // bytes per stage
+constexpr int kTmaSmem = kTmaStages * kTmaChunk;
+
+// First split s whose byte range ends after x (off[] is non-decreasing).
+__device__ __forceinline__ int first_split_after(const GatherArgs &a, int64_t x)
+{
+    int lo = 0, hi = a.nsplit;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (a.off[mid + 1] <= x) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// Piece of split s inside region [x0, x1) of rank r's shard: shard bytes
+// [p0, p1) and their destination byte offset d0 in every output.
+__device__ __forceinline__ bool piece_of(const GatherArgs &a, int r, int s, int64_t x0, int64_t x1,
+                                         int64_t &p0, int64_t &p1, int64_t &d0)
+{
+    const int64_t o = a.off[s], e = a.off[s + 1];
+    p0 = o > x0 ? o : x0;
+    p1 = e < x1 ? e : x1;
+    if (p0 >= p1) return false;
+    d0 = o * a.W + (int64_t)r * (e - o) + (p0 - o);
+    return true;
+}
+
+template <class T>
+__device__ __forceinline__ T ld_stream(const T *p) { return __ldcs(p); }
+template <class T>
+__device__ __forceinline__ void st_stream(T *p, T v) { __stcs(p, v); }
+
+// Copy n words of type T from src to every materialised output at byte
+// offset doff, using threads [tid0, tid0 + nthr) of the block.
+template <class T, int U>
+__device__ __forceinline__ void push_words(const GatherArgs &a, const char *src, int64_t doff,
+                                           int64_t n, int tid, int nthr)
+{
+    const T *s = reinterpret_cast<const T *>(src);
+    for (int64_t base = tid; base < n; base += (int64_t)nthr * U) {
+        T x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t i = base + (int64_t)u * nthr;
+            if (i < n) x[u] = ld_stream(s + i);
+        }
+        for (int q = 0; q < a.nout; ++q) {
+            T *d = reinterpret_cast<T *>(static_cast<char *>(a.out[a.qlist[q]]) + doff);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = base + (int64_t)u * nthr;
+                if (i < n) st_stream(d + i, x[u]);
+            }
+        }
+    }
+}
+
+// Copy len bytes (a whole number of elements) with the widest word both
+// sides' alignment allows.  Output bases are 16-byte aligned (checked on the
+// host), so only the offsets and the length decide.
+__device__ __forceinline__ void push_bytes(const GatherArgs &a, const char *src, int64_t doff,
+                                           int64_t len, int tid, int nthr)
+{
+    const uint64_t mis = (uint64_t)(uintptr_t)src | (uint64_t)doff | (uint64_t)len;
+    if ((mis & 15) == 0) push_words<uint4, 4>(a, src, doff, len >> 4, tid, nthr);
+    else if ((mis & 7) == 0) push_words<uint2, 4>(a, src, doff, len >> 3, tid, nthr);
+    else if ((mis & 3) == 0) push_words<unsigned int, 4>(a, src, doff, len >> 2, tid, nthr);
+    else push_words<unsigned short, 4>(a, src, doff, len >> 1, tid, nthr);
+}
+
+// ------------------------------------------------------------------ ldst engine
+__global__ void __launch_bounds__(kLdstThreads) gather_kernel_ldst(const __grid_constant__ GatherArgs a)
+{
+    __shared__ int s_ok;
+    const int r = blockIdx.x / a.B;
+    const int b = blockIdx.x - r * a.B;
+    if (b == 0) emit(a.sig, RR_BARRIER_ARRIVE, r, 0);
+    if (!wait(a.sig, RR_BARRIER_ARRIVE, r, 0, &s_ok)) return;
+
+    int64_t x0, x1;
+    byte_region(a.off[a.nsplit], a.B, b, x0, x1);
+    const char *src = static_cast<const char *>(a.src[r]);
+    if (x0 < x1) {
+        for (int s = first_split_after(a, x0); s < a.nsplit && a.off[s] < x1; ++s) {
+            int64_t p0, p1, d0;
+            if (piece_of(a, r, s, x0, x1, p0, p1, d0))
+                push_bytes(a, src + p0, d0, p1 - p0, threadIdx.x, kLdstThreads);
+        }
+    }
+    emit(a.sig, RR_BARRIER_END, r, b);
+    wait(a.sig, RR_BARRIER_END, r, b, &s_ok);
+}
+
+// ------------------------------------------------------------------ tma engine
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(sdst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// The part of piece s the bulk engine takes: both ends 16-byte aligned.
+__device__ __forceinline__ bool bulk_part(const GatherArgs &a, int r, int s, int64_t x0, int64_t x1,
+                                          int64_t &p0, int64_t &pend, int64_t &d0)
+{
+    int64_t p1;
+    if (!piece_of(a, r, s, x0, x1, p0, p1, d0)) return false;
+    if ((p0 & 15) || (d0 & 15)) return false;
+    pend = p0 + ((p1 - p0) & ~(int64_t)15);
+    return pend > p0;
+}
+
+// Bounded wait for the load of a stage; false after the pad's timeout.
+__device__ __forceinline__ bool stage_wait(const GatherArgs &a, uint64_t *bar, uint32_t parity)
+{
+    const uint64_t t0 = global_ns();
+    for (uint32_t spins = 0; !mbar_try_wait(bar, parity); ++spins) {
+        if ((spins & 255u) == 255u &&
+            ((global_ns() - t0) > a.sig.timeout_ns || spins > a.sig.max_spins))
+            return false;
+    }
+    return true;
+}
+
+__global__ void __launch_bounds__(kTmaThreads) gather_kernel_tma(const __grid_constant__ GatherArgs a)
+{
+    extern __shared__ __align__(128) unsigned char stage_mem[];
+    __shared__ __align__(8) uint64_t full[kTmaStages];
+    __shared__ int s_ok;
+    const int r = blockIdx.x / a.B;
+    const int b = blockIdx.x - r * a.B;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kTmaStages; ++i) mbar_init(&full[i], 1);
+        fence_mbar_init();
+    }
+    if (b == 0) emit(a.sig, RR_BARRIER_ARRIVE, r, 0);
+    else __syncthreads();
+    if (!wait(a.sig, RR_BARRIER_ARRIVE, r, 0, &s_ok)) return;
+
+    int64_t x0, x1;
+    byte_region(a.off[a.nsplit], a.B, b, x0, x1);
+    const char *src = static_cast<const char *>(a.src[r]);
+    const int sfirst = x0 < x1 ? first_split_after(a, x0) : a.nsplit;
+
+    if (threadIdx.x >= 32) {
+        // Everything the bulk engine does not take.
+        const int tid = threadIdx.x - 32, nthr = kTmaThreads - 32;
+        for (int s = sfirst; s < a.nsplit && a.off[s] < x1; ++s) {
+            int64_t p0, p1, d0, q0, qend, e0;
+            if (!piece_of(a, r, s, x0, x1, p0, p1, d0)) continue;
+            if (bulk_part(a, r, s, x0, x1, q0, qend, e0))
+                push_bytes(a, src + qend, d0 + (qend - p0), p1 - qend, tid, nthr);
+            else
+                push_bytes(a, src + p0, d0, p1 - p0, tid, nthr);
+        }
+    } else if (threadIdx.x == 0) {
+        // Chunk iterator over the bulk parts of the region's pieces.
+        int s = sfirst - 1;
+        int64_t pos = 0, pend = 0, dpos = 0;
+        auto next = [&](int64_t &cs, int64_t &cd, uint32_t &cl) -> bool {
+            while (pos >= pend) {
+                ++s;
+                if (s >= a.nsplit || a.off[s] >= x1) return false;
+                int64_t p0, pe, d0;
+                if (bulk_part(a, r, s, x0, x1, p0, pe, d0)) {
+                    pos = p0;
+                    pend = pe;
+                    dpos = d0;
+                }
+            }
+            const int64_t left = pend - pos;
+            cl = (uint32_t)(left < kTmaChunk ? left : kTmaChunk);
+            cs = pos;
+            cd = dpos;
+            pos += cl;
+            dpos += cl;
+            return true;
+        };
+        int64_t dst_of[kTmaStages];
+        uint32_t len_of[kTmaStages];
+        auto issue = [&](int k, int64_t cs, int64_t cd, uint32_t cl) {
+            const int st = k % kTmaStages;
+            dst_of[st] = cd;
+            len_of[st] = cl;
+            mbar_expect_tx(&full[st], cl);
+            bulk_load(stage_mem + (size_t)st * kTmaChunk, src + cs, cl, &full[st]);
+        };
+        int nissued = 0;
+        {
+            int64_t cs, cd;
+            uint32_t cl;
+            while (nissued < kTmaStages && next(cs, cd, cl)) issue(nissued++, cs, cd, cl);
+        }
+        bool ok = true;
+        for (int k = 0; k < nissued; ++k) {
+            const int st = k % kTmaStages;
+            if (!stage_wait(a, &full[st], (uint32_t)(k / kTmaStages) & 1u)) {
+                ok = false;
+                // Let the loads already in flight land before this block's
+                // shared memory can be handed to anyone else.
+                for (int j = k + 1; j < nissued; ++j)
+                    (void)stage_wait(a, &full[j % kTmaStages], (uint32_t)(j / kTmaStages) & 1u);
+                break;
+            }
+            fence_async_shared();
+            for (int q = 0; q < a.nout; ++q)
+                bulk_store(static_cast<char *>(a.out[a.qlist[q]]) + dst_of[st],
+                           stage_mem + (size_t)st * kTmaChunk, len_of[st]);
+            bulk_commit();
+            if (k >= 1) {
+                int64_t cs, cd;
+                uint32_t cl;
+                if (next(cs, cd, cl)) {
+                    bulk_wait_read_1();  // chunk k-1's stores have read their stage
+                    issue(nissued++, cs, cd, cl);
+                }
+            }
+        }
+        bulk_wait_all();
+        fence_async_global();
+        if (!ok) record_timeout(a.sig, RR_BARRIER_END, r, b);
+    }
+    emit(a.sig, RR_BARRIER_END, r, b);
+    wait(a.sig, RR_BARRIER_END, r, b, &s_ok);
+}
+
+KernelChoice gather_kernel_for(int engine)
+{
+    if (engine == 2) return KernelChoice{(const void *)gather_kernel_tma, kTmaThreads, kTmaSmem};
+    return KernelChoice{(const void *)gather_kernel_ldst, kLdstThreads, 0};
+}
+
+}  // namespace rr

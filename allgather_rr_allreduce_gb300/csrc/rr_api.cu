@@ -1,0 +1,527 @@
+// C-ABI host layer (include/rr.h): argument checks, signal pads, the choice
+// of blocks per rank, and one cooperative launch per call.
+//
+// No call here allocates, synchronises or copies to the device except
+// rr_signal_pad_create / _destroy / _status.  Pointer arrays are copied by
+// value into the kernel's parameter block.  Argument checks come before any
+// CUDA call, so they also run on a machine without a GPU.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "rr_internal.h"
+
+struct rr_signal_pad {
+    int device;
+    int W;
+    int Bmax;
+    uint64_t timeout_ns;
+    uint32_t *flags;   // device
+    uint32_t *status;  // device, rr::kStatusWords words
+    uint32_t gen;      // generation of the last call (0 = none yet)
+    int inject;        // -1 or rank*4 + barrier
+    int blocks_override;
+    int engine;        // 0 auto, 1 ldst, 2 tma
+    int last_grid;
+    int last_B;
+    int last_engine;
+    uint32_t timeout_info[4];  // barrier, rank, block, generation of the last cleared timeout
+};
+
+namespace {
+
+thread_local char g_err[512];
+
+rr_status fail(rr_status s, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+rr_status ok()
+{
+    g_err[0] = 0;
+    return RR_OK;
+}
+
+rr_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(RR_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+int elem_bytes(rr_dtype d)
+{
+    switch (d) {
+    case RR_BF16:
+    case RR_FP16: return 2;
+    case RR_FP32:
+    case RR_INT32: return 4;
+    default: return 0;
+    }
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Span {
+    uintptr_t lo, hi;
+};
+Span span_of(const void *p, int64_t bytes)
+{
+    uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return Span{a, a + (uintptr_t)bytes};
+}
+bool overlaps(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi && a.lo < a.hi && b.lo < b.hi; }
+
+// ---------------------------------------------------------------- device info
+std::mutex g_mu;
+std::map<int, int> g_sms;                               // device -> SM count
+std::map<std::pair<int, const void *>, int> g_occ;      // (device, kernel) -> blocks per SM
+
+rr_status resident_blocks(int dev, const rr::KernelChoice &k, int *out)
+{
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto sit = g_sms.find(dev);
+    if (sit == g_sms.end()) {
+        int sms = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(multiProcessorCount)");
+        sit = g_sms.emplace(dev, sms).first;
+    }
+    auto key = std::make_pair(dev, k.fn);
+    auto oit = g_occ.find(key);
+    if (oit == g_occ.end()) {
+        if (k.smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(maxDynamicSharedMemorySize)");
+        }
+        int per_sm = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.fn, k.threads, k.smem);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        oit = g_occ.emplace(key, per_sm).first;
+    }
+    *out = oit->second * sit->second;
+    return RR_OK;
+}
+
+// Blocks per rank: enough that each block moves about kBytesPerBlock, no
+// more than the pad allows, and few enough that all W*B blocks are resident
+// at once (the ranks' blocks wait on each other, so every one of them must
+// be running).  A fixed count set on the pad overrides the first rule.
+constexpr int64_t kBytesPerBlock = 32 * 1024;
+
+rr_status plan_blocks(rr_signal_pad *pad, const rr::KernelChoice &k, int W, int64_t total_bytes,
+                      int *B)
+{
+    int resident = 0;
+    rr_status st = resident_blocks(pad->device, k, &resident);
+    if (st != RR_OK) return st;
+    int cap = resident / W;
+    if (cap < 1) return fail(RR_ERR_TOO_MANY_BLOCKS, "%d ranks do not fit on the device at once", W);
+    if (cap > pad->Bmax) cap = pad->Bmax;
+    if (pad->blocks_override > 0) {
+        if (pad->blocks_override > cap)
+            return fail(RR_ERR_TOO_MANY_BLOCKS,
+                        "blocks_per_rank=%d exceeds the %d blocks per rank that can run at once here",
+                        pad->blocks_override, cap);
+        *B = pad->blocks_override;
+        return RR_OK;
+    }
+    int64_t want = (total_bytes + (int64_t)W * kBytesPerBlock - 1) / ((int64_t)W * kBytesPerBlock);
+    if (want < 1) want = 1;
+    *B = (int)(want < cap ? want : cap);
+    return RR_OK;
+}
+
+rr::SignalArgs signal_args(rr_signal_pad *pad)
+{
+    rr::SignalArgs s;
+    s.flags = pad->flags;
+    s.status = pad->status;
+    s.timeout_ns = pad->timeout_ns;
+    const uint64_t spins = pad->timeout_ns / 64 + 4096;
+    s.max_spins = spins > 0xffffffffull ? 0xffffffffu : (uint32_t)spins;
+    pad->gen += 1;
+    if (pad->gen == 0) pad->gen = 2;  // never 0 (the pad starts zeroed); keep the parity
+    s.g = pad->gen;
+    s.W = pad->W;
+    s.Bmax = pad->Bmax;
+    s.inject = pad->inject;
+    return s;
+}
+
+template <class Args>
+rr_status launch(rr_signal_pad *pad, const rr::KernelChoice &k, int grid, const Args &args,
+                 cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)k.threads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)k.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *params[1] = {const_cast<Args *>(&args)};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, k.fn, params);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC");
+    pad->last_grid = grid;
+    return ok();
+}
+
+rr_status check_pad(rr_signal_pad *pad, int W)
+{
+    if (!pad) return fail(RR_ERR_INVALID_ARG, "pad is NULL");
+    if (W < 1 || W > RR_MAX_WORLD) return fail(RR_ERR_INVALID_ARG, "world_size %d outside 1..%d", W, RR_MAX_WORLD);
+    if (W != pad->W) return fail(RR_ERR_INVALID_ARG, "world_size %d but the pad was made for %d", W, pad->W);
+    return RR_OK;
+}
+
+rr_status check_device(rr_signal_pad *pad)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != pad->device)
+        return fail(RR_ERR_WRONG_DEVICE, "current device %d, pad lives on device %d", dev, pad->device);
+    return RR_OK;
+}
+
+rr_status allreduce_common(bool twoshot, const void *const *inputs, void *const *rank_bufs,
+                           void *const *outputs, int W, int64_t numel, rr_dtype dtype, int copy_mode,
+                           rr_signal_pad *pad, cudaStream_t stream)
+{
+    rr_status st = check_pad(pad, W);
+    if (st != RR_OK) return st;
+    const int eb = elem_bytes(dtype);
+    if (eb == 0) return fail(RR_ERR_UNSUPPORTED_DTYPE, "dtype %d", (int)dtype);
+    if (numel < 0 || numel > ((int64_t)1 << 40)) return fail(RR_ERR_INVALID_ARG, "numel %lld", (long long)numel);
+    if (!rank_bufs || !outputs) return fail(RR_ERR_INVALID_ARG, "rank_bufs / outputs array is NULL");
+    if (copy_mode && !inputs) return fail(RR_ERR_INVALID_ARG, "copy_mode needs the inputs array");
+    const int64_t bytes = numel * eb;
+    int nout = 0;
+    for (int r = 0; r < W; ++r) {
+        if (!rank_bufs[r]) return fail(RR_ERR_INVALID_ARG, "rank_bufs[%d] is NULL", r);
+        if (!aligned16(rank_bufs[r])) return fail(RR_ERR_ALIGNMENT, "rank_bufs[%d] not 16-byte aligned", r);
+        if (copy_mode) {
+            if (!inputs[r]) return fail(RR_ERR_INVALID_ARG, "inputs[%d] is NULL", r);
+            if (!aligned16(inputs[r])) return fail(RR_ERR_ALIGNMENT, "inputs[%d] not 16-byte aligned", r);
+        }
+        if (outputs[r]) {
+            if (!aligned16(outputs[r])) return fail(RR_ERR_ALIGNMENT, "outputs[%d] not 16-byte aligned", r);
+            ++nout;
+        } else if (twoshot) {
+            return fail(RR_ERR_INVALID_ARG, "two-shot needs every output; outputs[%d] is NULL", r);
+        }
+    }
+    if (nout == 0) return fail(RR_ERR_INVALID_ARG, "no output is materialised");
+    for (int i = 0; i < W; ++i) {
+        const Span bi = span_of(rank_bufs[i], bytes);
+        for (int j = 0; j < W; ++j) {
+            if (j > i && overlaps(bi, span_of(rank_bufs[j], bytes)))
+                return fail(RR_ERR_ALIAS, "rank_bufs[%d] and rank_bufs[%d] overlap", i, j);
+            if (copy_mode && overlaps(bi, span_of(inputs[j], bytes)))
+                return fail(RR_ERR_ALIAS, "rank_bufs[%d] and inputs[%d] overlap", i, j);
+            if (outputs[j] && overlaps(bi, span_of(outputs[j], bytes)))
+                return fail(RR_ERR_ALIAS, "rank_bufs[%d] and outputs[%d] overlap", i, j);
+        }
+        if (!outputs[i]) continue;
+        const Span oi = span_of(outputs[i], bytes);
+        for (int j = 0; j < W; ++j) {
+            if (j > i && outputs[j] && overlaps(oi, span_of(outputs[j], bytes)))
+                return fail(RR_ERR_ALIAS, "outputs[%d] and outputs[%d] overlap", i, j);
+            if (copy_mode && overlaps(oi, span_of(inputs[j], bytes)))
+                return fail(RR_ERR_ALIAS, "outputs[%d] and inputs[%d] overlap", i, j);
+        }
+    }
+    if (numel == 0) return ok();
+    st = check_device(pad);
+    if (st != RR_OK) return st;
+
+    const rr::KernelChoice k = twoshot ? rr::twoshot_kernel_for(dtype, W) : rr::oneshot_kernel_for(dtype, W);
+    int64_t moved = twoshot ? bytes * (W + 1) + (int64_t)(W - 1) * bytes * 2
+                            : (int64_t)nout * bytes * (W + 1);
+    if (copy_mode) moved += 2 * (int64_t)W * bytes;
+    int B = 0;
+    st = plan_blocks(pad, k, W, moved, &B);
+    if (st != RR_OK) return st;
+
+    rr::ReduceArgs a;
+    std::memset(&a, 0, sizeof a);
+    for (int r = 0; r < W; ++r) {
+        a.in[r] = copy_mode ? inputs[r] : nullptr;
+        a.buf[r] = rank_bufs[r];
+        a.out[r] = outputs[r];
+        if (outputs[r]) a.qlist[a.nout++] = r;
+    }
+    a.numel = numel;
+    a.nvec = bytes / 16;
+    a.W = W;
+    a.B = B;
+    a.copy_mode = copy_mode ? 1 : 0;
+    a.sig = signal_args(pad);
+    pad->last_B = B;
+    pad->last_engine = 1;
+    return launch(pad, k, W * B, a, stream);
+}
+
+rr_status gather_common(const void *const *rank_bufs, void *const *outputs, int W,
+                        const int64_t *splits, int nsplit, rr_dtype dtype, rr_signal_pad *pad,
+                        cudaStream_t stream)
+{
+    rr_status st = check_pad(pad, W);
+    if (st != RR_OK) return st;
+    const int eb = elem_bytes(dtype);
+    if (eb == 0) return fail(RR_ERR_UNSUPPORTED_DTYPE, "dtype %d", (int)dtype);
+    if (nsplit < 0 || nsplit > RR_MAX_SPLITS)
+        return fail(RR_ERR_INVALID_ARG, "num_splits %d outside 0..%d", nsplit, RR_MAX_SPLITS);
+    if (nsplit > 0 && !splits) return fail(RR_ERR_INVALID_ARG, "split_sizes is NULL");
+    if (!rank_bufs || !outputs) return fail(RR_ERR_INVALID_ARG, "rank_bufs / outputs array is NULL");
+    rr::GatherArgs a;
+    std::memset(&a, 0, sizeof a);
+    int64_t total = 0;
+    a.off[0] = 0;
+    for (int s = 0; s < nsplit; ++s) {
+        if (splits[s] < 0) return fail(RR_ERR_INVALID_ARG, "split_sizes[%d] = %lld", s, (long long)splits[s]);
+        total += splits[s];
+        if (total > ((int64_t)1 << 40)) return fail(RR_ERR_INVALID_ARG, "shard too large");
+        a.off[s + 1] = total * eb;
+    }
+    const int64_t shard = total * eb;
+    const int64_t outb = shard * W;
+    int nout = 0;
+    for (int r = 0; r < W; ++r) {
+        if (!rank_bufs[r]) return fail(RR_ERR_INVALID_ARG, "rank_bufs[%d] is NULL", r);
+        if (!aligned16(rank_bufs[r])) return fail(RR_ERR_ALIGNMENT, "rank_bufs[%d] not 16-byte aligned", r);
+        if (outputs[r]) {
+            if (!aligned16(outputs[r])) return fail(RR_ERR_ALIGNMENT, "outputs[%d] not 16-byte aligned", r);
+            ++nout;
+        }
+    }
+    if (nout == 0) return fail(RR_ERR_INVALID_ARG, "no output is materialised");
+    for (int i = 0; i < W; ++i) {
+        if (!outputs[i]) continue;
+        const Span oi = span_of(outputs[i], outb);
+        for (int j = 0; j < W; ++j) {
+            if (j > i && outputs[j] && overlaps(oi, span_of(outputs[j], outb)))
+                return fail(RR_ERR_ALIAS, "outputs[%d] and outputs[%d] overlap", i, j);
+            if (overlaps(oi, span_of(rank_bufs[j], shard)))
+                return fail(RR_ERR_ALIAS, "outputs[%d] and rank_bufs[%d] overlap", i, j);
+        }
+    }
+    if (shard == 0) return ok();
+    st = check_device(pad);
+    if (st != RR_OK) return st;
+
+    const int engine = pad->engine == 0 ? 2 : pad->engine;
+    const rr::KernelChoice k = rr::gather_kernel_for(engine);
+    int B = 0;
+    st = plan_blocks(pad, k, W, shard * W + shard * W * nout, &B);
+    if (st != RR_OK) return st;
+    for (int r = 0; r < W; ++r) {
+        a.src[r] = rank_bufs[r];
+        a.out[r] = outputs[r];
+        if (outputs[r]) a.qlist[a.nout++] = r;
+    }
+    a.W = W;
+    a.B = B;
+    a.nsplit = nsplit;
+    a.sig = signal_args(pad);
+    pad->last_B = B;
+    pad->last_engine = engine;
+    return launch(pad, k, W * B, a, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+rr_status rr_signal_pad_create(int world_size, int max_blocks_per_rank, uint64_t timeout_ns,
+                               rr_signal_pad **out)
+{
+    if (!out) return fail(RR_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (world_size < 1 || world_size > RR_MAX_WORLD)
+        return fail(RR_ERR_INVALID_ARG, "world_size %d outside 1..%d", world_size, RR_MAX_WORLD);
+    if (max_blocks_per_rank < 0 || max_blocks_per_rank > 65536)
+        return fail(RR_ERR_INVALID_ARG, "max_blocks_per_rank %d", max_blocks_per_rank);
+    const int Bmax = max_blocks_per_rank ? max_blocks_per_rank : rr::kDefaultMaxBlocks;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    const size_t nflags = (size_t)world_size * rr::kNumBarriers * 2 * (size_t)Bmax * (size_t)world_size;
+    const size_t bytes = (nflags + rr::kStatusWords) * sizeof(uint32_t);
+    void *mem = nullptr;
+    e = cudaMalloc(&mem, bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(signal pad)");
+    e = cudaMemset(mem, 0, bytes);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        cudaFree(mem);
+        return cuda_fail(e, "zeroing the signal pad");
+    }
+    rr_signal_pad *p = new rr_signal_pad;
+    std::memset(p, 0, sizeof *p);
+    p->device = dev;
+    p->W = world_size;
+    p->Bmax = Bmax;
+    p->timeout_ns = timeout_ns ? timeout_ns : rr::kDefaultTimeoutNs;
+    p->flags = static_cast<uint32_t *>(mem);
+    p->status = p->flags + nflags;
+    p->inject = -1;
+    *out = p;
+    return ok();
+}
+
+rr_status rr_signal_pad_destroy(rr_signal_pad *pad)
+{
+    if (!pad) return ok();
+    int prev = -1;
+    cudaGetDevice(&prev);
+    cudaSetDevice(pad->device);
+    cudaError_t e = cudaDeviceSynchronize();
+    cudaError_t f = cudaFree(pad->flags);
+    if (prev >= 0) cudaSetDevice(prev);
+    delete pad;
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    if (f != cudaSuccess) return cuda_fail(f, "cudaFree(signal pad)");
+    return ok();
+}
+
+rr_status rr_signal_pad_status(rr_signal_pad *pad, cudaStream_t stream)
+{
+    if (!pad) return fail(RR_ERR_INVALID_ARG, "pad is NULL");
+    rr_status st = check_device(pad);
+    if (st != RR_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    uint32_t words[rr::kStatusWords];
+    e = cudaMemcpy(words, pad->status, sizeof words, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
+    if (words[rr::kStErr] == 0 && words[rr::kStAbort] == 0) return ok();
+    pad->timeout_info[0] = words[rr::kStBarrier];
+    pad->timeout_info[1] = words[rr::kStRank];
+    pad->timeout_info[2] = words[rr::kStBlock];
+    pad->timeout_info[3] = words[rr::kStGen];
+    e = cudaMemsetAsync(pad->status, 0, sizeof words, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the status");
+    const rr_status dev_status = words[rr::kStErr] ? (rr_status)words[rr::kStErr] : RR_ERR_TIMEOUT;
+    return fail(dev_status, "barrier %u timed out: waiting rank %u, block %u, generation %u",
+                words[rr::kStBarrier], words[rr::kStRank], words[rr::kStBlock], words[rr::kStGen]);
+}
+
+rr_status rr_signal_pad_timeout_info(rr_signal_pad *pad, int *barrier, int *rank, int *block,
+                                     uint32_t *generation)
+{
+    if (!pad) return fail(RR_ERR_INVALID_ARG, "pad is NULL");
+    if (barrier) *barrier = (int)pad->timeout_info[0];
+    if (rank) *rank = (int)pad->timeout_info[1];
+    if (block) *block = (int)pad->timeout_info[2];
+    if (generation) *generation = pad->timeout_info[3];
+    return ok();
+}
+
+rr_status rr_signal_pad_set_option(rr_signal_pad *pad, rr_option opt, int64_t value)
+{
+    if (!pad) return fail(RR_ERR_INVALID_ARG, "pad is NULL");
+    switch (opt) {
+    case RR_OPT_TIMEOUT_NS:
+        if (value <= 0) return fail(RR_ERR_INVALID_ARG, "timeout must be positive");
+        pad->timeout_ns = (uint64_t)value;
+        return ok();
+    case RR_OPT_BLOCKS_PER_RANK:
+        if (value < 0 || value > pad->Bmax)
+            return fail(RR_ERR_INVALID_ARG, "blocks_per_rank %lld outside 0..%d", (long long)value, pad->Bmax);
+        pad->blocks_override = (int)value;
+        return ok();
+    case RR_OPT_GATHER_ENGINE:
+        if (value < 0 || value > 2) return fail(RR_ERR_INVALID_ARG, "engine %lld", (long long)value);
+        pad->engine = (int)value;
+        return ok();
+    case RR_OPT_INJECT_SKIP:
+        if (value < -1 || value >= (int64_t)pad->W * rr::kNumBarriers)
+            return fail(RR_ERR_INVALID_ARG, "inject %lld", (long long)value);
+        pad->inject = (int)value;
+        return ok();
+    default: return fail(RR_ERR_INVALID_ARG, "option %d cannot be set", (int)opt);
+    }
+}
+
+rr_status rr_signal_pad_get_option(rr_signal_pad *pad, rr_option opt, int64_t *value)
+{
+    if (!pad || !value) return fail(RR_ERR_INVALID_ARG, "pad or value is NULL");
+    switch (opt) {
+    case RR_OPT_TIMEOUT_NS: *value = (int64_t)pad->timeout_ns; break;
+    case RR_OPT_BLOCKS_PER_RANK: *value = pad->blocks_override; break;
+    case RR_OPT_GATHER_ENGINE: *value = pad->engine; break;
+    case RR_OPT_INJECT_SKIP: *value = pad->inject; break;
+    case RR_OPT_GENERATION: *value = pad->gen; break;
+    case RR_OPT_LAST_GRID: *value = pad->last_grid; break;
+    case RR_OPT_LAST_BLOCKS_PER_RANK: *value = pad->last_B; break;
+    case RR_OPT_LAST_ENGINE: *value = pad->last_engine; break;
+    case RR_OPT_WORLD_SIZE: *value = pad->W; break;
+    case RR_OPT_MAX_BLOCKS_PER_RANK: *value = pad->Bmax; break;
+    default: return fail(RR_ERR_INVALID_ARG, "unknown option %d", (int)opt);
+    }
+    return ok();
+}
+
+rr_status rr_allreduce_oneshot(const void *const *inputs, void *const *rank_bufs, void *const *outputs,
+                               int world_size, int64_t numel, rr_dtype dtype, int copy_mode,
+                               rr_signal_pad *pad, cudaStream_t stream)
+{
+    return allreduce_common(false, inputs, rank_bufs, outputs, world_size, numel, dtype, copy_mode, pad,
+                            stream);
+}
+
+rr_status rr_allreduce_twoshot(const void *const *inputs, void *const *rank_bufs, void *const *outputs,
+                               int world_size, int64_t numel, rr_dtype dtype, int copy_mode,
+                               rr_signal_pad *pad, cudaStream_t stream)
+{
+    return allreduce_common(true, inputs, rank_bufs, outputs, world_size, numel, dtype, copy_mode, pad,
+                            stream);
+}
+
+rr_status rr_allgather(const void *const *rank_bufs, void *const *outputs, int world_size,
+                       int64_t numel_per_rank, rr_dtype dtype, rr_signal_pad *pad, cudaStream_t stream)
+{
+    if (numel_per_rank < 0) return fail(RR_ERR_INVALID_ARG, "numel_per_rank %lld", (long long)numel_per_rank);
+    const int64_t split = numel_per_rank;
+    return gather_common(rank_bufs, outputs, world_size, &split, 1, dtype, pad, stream);
+}
+
+rr_status rr_allgather_param_contiguous(const void *const *rank_bufs, void *const *outputs,
+                                        int world_size, const int64_t *split_sizes, int num_splits,
+                                        rr_dtype dtype, rr_signal_pad *pad, cudaStream_t stream)
+{
+    return gather_common(rank_bufs, outputs, world_size, split_sizes, num_splits, dtype, pad, stream);
+}
+
+const char *rr_status_string(rr_status s)
+{
+    switch (s) {
+    case RR_OK: return "RR_OK";
+    case RR_ERR_INVALID_ARG: return "RR_ERR_INVALID_ARG";
+    case RR_ERR_UNSUPPORTED_DTYPE: return "RR_ERR_UNSUPPORTED_DTYPE";
+    case RR_ERR_ALIGNMENT: return "RR_ERR_ALIGNMENT";
+    case RR_ERR_ALIAS: return "RR_ERR_ALIAS";
+    case RR_ERR_TOO_MANY_BLOCKS: return "RR_ERR_TOO_MANY_BLOCKS";
+    case RR_ERR_CUDA: return "RR_ERR_CUDA";
+    case RR_ERR_TIMEOUT: return "RR_ERR_TIMEOUT";
+    case RR_ERR_WRONG_DEVICE: return "RR_ERR_WRONG_DEVICE";
+    default: return "RR_ERR_UNKNOWN";
+    }
+}
+
+const char *rr_last_error(void) { return g_err; }
+
+}  // extern "C"

@@ -1,0 +1,137 @@
+// Internal declarations shared by the C-ABI host layer (rr_api.cu) and the
+// kernels (rr_allreduce.cu, rr_allgather.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "rr.h"
+
+#if defined(__CUDACC__)
+#define RR_HD __host__ __device__ __forceinline__
+#else
+#define RR_HD inline
+#endif
+
+namespace rr {
+
+constexpr int kNumBarriers = 4;       // rr_barrier values
+constexpr int kDefaultMaxBlocks = 1024;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+// Words of the device status block of a pad.
+enum StatusWord : int {
+    kStErr = 0,      // first rr_status recorded by the device (sticky)
+    kStAbort = 1,    // non-zero: every barrier wait gives up at once
+    kStBarrier = 2,  // where the first timeout happened ...
+    kStRank = 3,
+    kStBlock = 4,
+    kStGen = 5,
+    kStatusWords = 8
+};
+
+// Everything a kernel needs to take part in the pad's barriers.
+struct SignalArgs {
+    uint32_t *flags;     // [W listener][kNumBarriers][2][Bmax][W emitter]
+    uint32_t *status;    // kStatusWords words
+    uint64_t timeout_ns; // per wait
+    uint32_t max_spins;  // iteration backstop of a wait, in case the timer misbehaves
+    uint32_t g;          // generation value of this call (never 0)
+    int W;
+    int Bmax;
+    int inject;          // -1, or rank*4 + barrier whose flags are never emitted
+};
+
+// One-shot and two-shot allreduce.
+struct ReduceArgs {
+    const void *in[RR_MAX_WORLD];  // copy_mode sources
+    void *buf[RR_MAX_WORLD];       // registered rank buffers
+    void *out[RR_MAX_WORLD];       // outputs (may be null for one-shot)
+    int64_t numel;                 // elements per rank
+    int64_t nvec;                  // whole 16-byte vectors per rank
+    int W;
+    int B;                         // blocks per rank
+    int copy_mode;
+    int nout;                      // number of materialised outputs
+    int qlist[RR_MAX_WORLD];       // their ranks, ascending
+    SignalArgs sig;
+};
+
+// Rank-major and param-contiguous allgather (rank-major = one split).
+struct GatherArgs {
+    const void *src[RR_MAX_WORLD];     // rank shards
+    void *out[RR_MAX_WORLD];           // outputs (null = not materialised)
+    int64_t off[RR_MAX_SPLITS + 1];    // byte offset of param s in a shard; off[nsplit] = shard bytes
+    int W;
+    int B;
+    int nsplit;
+    int nout;
+    int qlist[RR_MAX_WORLD];
+    SignalArgs sig;
+};
+
+// ---------------------------------------------------------------- partition
+// Work is cut into 256-byte granules (16 vectors of 16 bytes) so that block
+// boundaries never split a 128-byte line between two blocks.
+constexpr int64_t kGranuleVec = 16;
+constexpr int64_t kGranuleBytes = kGranuleVec * 16;
+
+RR_HD int64_t split_point(int64_t n, int64_t parts, int64_t i) { return (n * i) / parts; }
+
+// Vectors [v0, v1) of part i when n vectors are split into `parts` runs of
+// whole granules (the last granule may be short).
+RR_HD void part_range(int64_t n, int64_t parts, int64_t i, int64_t &v0, int64_t &v1)
+{
+    const int64_t ng = (n + kGranuleVec - 1) / kGranuleVec;
+    int64_t a = split_point(ng, parts, i) * kGranuleVec;
+    int64_t b = split_point(ng, parts, i + 1) * kGranuleVec;
+    v0 = a < n ? a : n;
+    v1 = b < n ? b : n;
+}
+
+// Two-shot ownership: rank c owns vectors [c*C, min((c+1)*C, n)) where C is
+// ceil(granules / W) granules.
+RR_HD void owned_segment(int64_t n, int W, int c, int64_t &s0, int64_t &s1)
+{
+    const int64_t ng = (n + kGranuleVec - 1) / kGranuleVec;
+    const int64_t C = ((ng + W - 1) / W) * kGranuleVec;
+    int64_t a = C * c, b = C * (c + 1);
+    s0 = a < n ? a : n;
+    s1 = b < n ? b : n;
+}
+
+// Block b's chunk of rank c's owned segment.
+RR_HD void owned_chunk(int64_t n, int W, int B, int c, int b, int64_t &v0, int64_t &v1)
+{
+    int64_t s0, s1;
+    owned_segment(n, W, c, s0, s1);
+    int64_t a, e;
+    part_range(s1 - s0, B, b, a, e);
+    v0 = s0 + a;
+    v1 = s0 + e;
+}
+
+// Region b (in bytes) of a shard of `bytes` bytes, in whole granules.
+RR_HD void byte_region(int64_t bytes, int B, int b, int64_t &x0, int64_t &x1)
+{
+    const int64_t ng = (bytes + kGranuleBytes - 1) / kGranuleBytes;
+    int64_t a = split_point(ng, B, b) * kGranuleBytes;
+    int64_t e = split_point(ng, B, b + 1) * kGranuleBytes;
+    x0 = a < bytes ? a : bytes;
+    x1 = e < bytes ? e : bytes;
+}
+
+// ---------------------------------------------------------------- launchers
+// Implemented in rr_allreduce.cu / rr_allgather.cu.  Each returns the kernel
+// to launch for the given element type and world size, with its block size
+// and dynamic shared memory.
+struct KernelChoice {
+    const void *fn;
+    int threads;
+    int smem;
+};
+KernelChoice oneshot_kernel_for(rr_dtype dtype, int W);
+KernelChoice twoshot_kernel_for(rr_dtype dtype, int W);
+KernelChoice gather_kernel_for(int engine);  // 1 = loads/stores, 2 = TMA bulk
+
+}  // namespace rr

@@ -1,0 +1,250 @@
+/*
+ * rr.h -- C ABI of the reduce/gather data movement inside a custom collective,
+ * for one GB300 (sm_103a) GPU.
+ *
+ * W "ranks" are emulated on one GPU: each rank's registered buffer is a plain
+ * device pointer into this GPU's own HBM, standing in for the peer (IPC /
+ * symmetric-memory) buffers a real multi-GPU collective would address.  One
+ * call launches one kernel that runs all W ranks' per-GPU work as W groups of
+ * blocks; the groups order themselves through a signal pad of generation
+ * flags in the same HBM.  No NCCL, no peer access and no host synchronisation
+ * happen on any call below except rr_signal_pad_create/_destroy/_status.
+ *
+ * Conventions for every entry point:
+ *  - Pointer arrays (inputs, rank_bufs, outputs) are HOST arrays of W device
+ *    pointers.  They are read during the call only (copied by value into the
+ *    kernel's parameters), so the caller may reuse them as soon as the call
+ *    returns.  The pointed-to device buffers are owned by the caller and must
+ *    stay valid until the work completes on `stream`.
+ *  - Every device pointer must be 16-byte aligned (RR_ERR_ALIGNMENT).  It may
+ *    point anywhere inside a larger allocation.  Any element count is
+ *    accepted, not only multiples of the 16-byte vector.
+ *  - Buffers are dense: rank r's data is `numel` consecutive elements.
+ *  - Outputs must not overlap any input, rank buffer or other output
+ *    (RR_ERR_ALIAS); rank buffers must not overlap each other.
+ *  - Argument errors are returned synchronously, before anything is
+ *    enqueued.  A barrier that times out on the device is recorded in the
+ *    pad (sticky) and read back with rr_signal_pad_status.
+ *  - Calls are asynchronous with respect to the host and ordered on
+ *    `stream` (a cudaStream_t; 0 is the legacy default stream).  A pad may be
+ *    used by one stream at a time: concurrent collectives need separate
+ *    pads, because a pad's flag slots and generation counter are shared
+ *    state (the lesson of the shared per-slot flag in "ccl: hierarchical
+ *    cross-node AllGather (intra-node SDMA + inter-node RDMA) #441", the
+ *    commit on concurrent param-contiguous scatters).
+ *  - Reductions accumulate in binary32 in rank order 0, 1, ..., W-1, starting
+ *    from rank 0's value, and round once to the element type (round to
+ *    nearest, ties to even; no flush of subnormals).  int32 sums wrap modulo
+ *    2^32.  Gathers copy raw bits.
+ */
+#ifndef RR_H
+#define RR_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RR_MAX_WORLD 16   /* largest W */
+#define RR_MAX_SPLITS 256 /* largest number of params in one param-contiguous call */
+
+typedef enum { RR_BF16 = 0, RR_FP16 = 1, RR_FP32 = 2, RR_INT32 = 3 } rr_dtype;
+
+typedef enum {
+    RR_OK = 0,
+    RR_ERR_INVALID_ARG = 1,       /* null pointer, W out of range, negative size, ... */
+    RR_ERR_UNSUPPORTED_DTYPE = 2,
+    RR_ERR_ALIGNMENT = 3,         /* a device pointer is not 16-byte aligned */
+    RR_ERR_ALIAS = 4,             /* buffers overlap where they must not */
+    RR_ERR_TOO_MANY_BLOCKS = 5,   /* the pad was created for fewer blocks per rank */
+    RR_ERR_CUDA = 6,              /* a CUDA runtime call failed; see rr_last_error */
+    RR_ERR_TIMEOUT = 7,           /* a device-side barrier wait ran out of time */
+    RR_ERR_WRONG_DEVICE = 8       /* the current device is not the pad's device */
+} rr_status;
+
+/* Barriers inside one call, used to name a barrier in fault injection and in
+ * the diagnostic of a timeout. */
+typedef enum {
+    RR_BARRIER_ARRIVE = 0, /* start, no staging: block 0 of every rank announces arrival */
+    RR_BARRIER_STAGE = 1,  /* start, copy_mode: block b of every rank has staged its chunk */
+    RR_BARRIER_MID = 2,    /* two-shot: block b of every rank has reduced its owned chunk */
+    RR_BARRIER_END = 3     /* end: block b of every rank is done with every peer buffer */
+} rr_barrier;
+
+/* Options of a pad (rr_signal_pad_set_option / rr_signal_pad_get_option). */
+typedef enum {
+    RR_OPT_TIMEOUT_NS = 0,      /* barrier wait limit in ns (default 2e9) */
+    RR_OPT_BLOCKS_PER_RANK = 1, /* 0 = automatic (default); else a fixed block count per rank */
+    RR_OPT_GATHER_ENGINE = 2,   /* 0 = automatic, 1 = 128-bit loads/stores, 2 = TMA bulk copies */
+    RR_OPT_INJECT_SKIP = 3,     /* fault injection: -1 = off; else rank*4 + barrier: that rank
+                                   never emits that barrier's flags, so peers time out */
+    /* read-only */
+    RR_OPT_GENERATION = 16,     /* generation flag value of the last call */
+    RR_OPT_LAST_GRID = 17,      /* blocks launched by the last call */
+    RR_OPT_LAST_BLOCKS_PER_RANK = 18,
+    RR_OPT_LAST_ENGINE = 19,    /* engine the last gather used (1 or 2) */
+    RR_OPT_WORLD_SIZE = 20,
+    RR_OPT_MAX_BLOCKS_PER_RANK = 21
+} rr_option;
+
+typedef struct rr_signal_pad rr_signal_pad; /* opaque, owned by the library */
+
+/*
+ * rr_signal_pad_create -- allocate the signal pad of one communicator.
+ *
+ * The pad is the array of 32-bit generation flags that the ranks' blocks
+ * exchange, as the `uint32_t** signals` of multi_gpu_barrier / block_barrier
+ * in "Question and suggestions about custom allreduce" (sglang discussion
+ * 2918), leizhao1234's first post: dimension 0 listens, the last dimension
+ * emits.  Layout here: [W listener][4 barriers][2 parities][blocks][W emitter]
+ * uint32 words on the current device, plus a status block.  Each call takes
+ * the next generation value g (a host counter, never 0) and writes g into
+ * slots of parity g & 1, so consecutive calls never share a slot
+ * ("offset = (flag % 2) ? world_size : 0" in the same post).
+ *
+ * world_size: W, 1..RR_MAX_WORLD.  max_blocks_per_rank: upper bound on
+ * blocks per rank any call on this pad may use (0 = 1024).  timeout_ns:
+ * barrier wait limit (0 = 2 s).  Allocates and zeroes device memory and
+ * synchronises the device once.  *out receives the pad.
+ */
+rr_status rr_signal_pad_create(int world_size, int max_blocks_per_rank, uint64_t timeout_ns,
+                               rr_signal_pad **out);
+
+/* Free the pad's device memory (synchronises the device first). NULL is a no-op. */
+rr_status rr_signal_pad_destroy(rr_signal_pad *pad);
+
+/*
+ * Synchronise `stream`, then return the pad's sticky device status: RR_OK, or
+ * RR_ERR_TIMEOUT if any barrier wait of an earlier call ran out of time.
+ * Reading the status clears it.  While a timeout is pending, every later call
+ * on the pad exits at its first barrier without writing outputs.
+ * rr_signal_pad_timeout_info gives where the first timeout happened.
+ */
+rr_status rr_signal_pad_status(rr_signal_pad *pad, cudaStream_t stream);
+
+/* Where the last cleared timeout happened: barrier, waiting rank, block, and
+ * the generation of the call.  Valid after rr_signal_pad_status returned
+ * RR_ERR_TIMEOUT. */
+rr_status rr_signal_pad_timeout_info(rr_signal_pad *pad, int *barrier, int *rank, int *block,
+                                     uint32_t *generation);
+
+rr_status rr_signal_pad_set_option(rr_signal_pad *pad, rr_option opt, int64_t value);
+rr_status rr_signal_pad_get_option(rr_signal_pad *pad, rr_option opt, int64_t *value);
+
+/*
+ * rr_allreduce_oneshot -- every rank reads all W rank buffers and writes the
+ * element-wise sum to its own output.
+ *
+ * Source: "Question and suggestions about custom allreduce" (sglang discussion
+ * 2918), the trt_reduce_internal.cu block comment quoted in yizhang2077's
+ * reply: each block (1) copies its chunk from local_input to the shareable
+ * buffer when copy_mode is on, (2) waits for the same block on every other
+ * GPU, (3) pulls the chunk from every GPU, sums it and writes local_output;
+ * with copy_mode off step 1 is skipped and only the arrival of every GPU is
+ * awaited.
+ *
+ * inputs:    W device pointers, rank r's local input (numel elements).  Read
+ *            only when copy_mode != 0 (may be NULL otherwise).
+ * rank_bufs: W device pointers, rank r's registered buffer (numel elements).
+ *            copy_mode != 0: the kernel stages inputs[r] into rank_bufs[r]
+ *            (overwritten).  copy_mode == 0: rank_bufs[r] already holds rank
+ *            r's data and is only read.
+ * outputs:   W device pointers, rank r's output (numel elements).  An entry
+ *            may be NULL: that rank's output is not materialised (its blocks
+ *            still stage, signal, and lend their bandwidth to the
+ *            materialised outputs of the same chunk).  At least one non-NULL.
+ * numel:     elements per rank (>= 0; 0 returns RR_OK without a launch).
+ * dtype:     RR_BF16, RR_FP16, RR_FP32 (binary32 accumulate) or RR_INT32.
+ * Barriers: ARRIVE (copy_mode off) or STAGE (copy_mode on) before the
+ * reduction, END after it, so that when the call completes on `stream` no rank
+ * still reads any peer buffer.
+ */
+rr_status rr_allreduce_oneshot(const void *const *inputs, void *const *rank_bufs,
+                               void *const *outputs, int world_size, int64_t numel,
+                               rr_dtype dtype, int copy_mode, rr_signal_pad *pad,
+                               cudaStream_t stream);
+
+/*
+ * rr_allreduce_twoshot -- reduce-scatter then allgather: rank r owns segment
+ * S_r of the message, reduces it from all W rank buffers into outputs[r][S_r],
+ * and after a barrier copies every other owner's reduced segment
+ * outputs[c][S_c] into outputs[r][S_c].
+ *
+ * Source: "Question and suggestions about custom allreduce" (sglang discussion
+ * 2918), leizhao1234's opening post (two-shot needs an arrival barrier and a
+ * block barrier between its two phases), and the owned-slice partition of
+ * multimem_all_reduce_kernel in "triton_multimem_all_reduce.py"
+ * (symm-mem-recipes): rank r covers 128-bit units [r*C, (r+1)*C) with
+ * C = ceil(units / W).  Here the owned segments are C 16-byte vectors (rounded
+ * up to whole 256-byte granules), the last segment short or empty, and the
+ * elements after the last whole vector are owned by rank W-1.
+ *
+ * Arguments as rr_allreduce_oneshot, except that every outputs[r] is required
+ * (peers read the reduced segments from it).  Barriers: ARRIVE or STAGE,
+ * MID between the phases, END.  Results are bit-identical to the one-shot.
+ */
+rr_status rr_allreduce_twoshot(const void *const *inputs, void *const *rank_bufs,
+                               void *const *outputs, int world_size, int64_t numel,
+                               rr_dtype dtype, int copy_mode, rr_signal_pad *pad,
+                               cudaStream_t stream);
+
+/*
+ * rr_allgather -- all_gather_into_tensor, rank-major: every materialised
+ * output q receives rank r's buffer at element offset r * numel_per_rank.
+ *
+ * Source: "ccl: hierarchical cross-node AllGather (intra-node SDMA +
+ * inter-node RDMA) #441", the PR description (an all_gather_into_tensor-
+ * compatible collective, bit-exact for bf16/fp16/fp32/int32).  Each rank
+ * pushes its own shard into every materialised output, as that PR's gather
+ * pushes straight into the destination.
+ *
+ * rank_bufs: W device pointers, rank r's shard (numel_per_rank elements).
+ * outputs:   W device pointers to W*numel_per_rank elements each, or NULL
+ *            (not materialised); at least one non-NULL.
+ * Raw bits are copied (any dtype; NaN payloads survive).  Barriers: ARRIVE,
+ * END (every push into an output has landed before its rank completes).
+ */
+rr_status rr_allgather(const void *const *rank_bufs, void *const *outputs, int world_size,
+                       int64_t numel_per_rank, rr_dtype dtype, rr_signal_pad *pad,
+                       cudaStream_t stream);
+
+/*
+ * rr_allgather_param_contiguous -- FSDP-style allgather into a [param][rank]
+ * output: rank r's shard is the concatenation of its pieces of params
+ * 0..S-1 (piece s has E_s = split_sizes[s] elements and starts at
+ * O_s = E_0 + ... + E_{s-1}); the piece lands at element O_s*W + r*E_s of
+ * every materialised output.
+ *
+ * Source: "ccl: hierarchical cross-node AllGather (intra-node SDMA +
+ * inter-node RDMA) #441", the commit adding enqueue_param_contiguous (rank r
+ * lands at O_s*W + r*E_s, from "dtype-elem splits"), and the following commit
+ * that loops all blocks and splits inside one launch instead of one launch
+ * per (node block, param).  One call here is one launch over every
+ * (rank, param) slot.  The node grouping G of that PR does not change where
+ * anything lands, so it is not an argument.
+ *
+ * split_sizes: HOST array of num_splits (0..RR_MAX_SPLITS) element counts,
+ *              each >= 0.  rank_bufs[r] holds sum(E_s) elements.
+ * outputs:     W device pointers to W*sum(E_s) elements each, or NULL.
+ * Raw bits are copied.  Barriers: ARRIVE, END.
+ */
+rr_status rr_allgather_param_contiguous(const void *const *rank_bufs, void *const *outputs,
+                                        int world_size, const int64_t *split_sizes,
+                                        int num_splits, rr_dtype dtype, rr_signal_pad *pad,
+                                        cudaStream_t stream);
+
+/* Name of a status code (static string). */
+const char *rr_status_string(rr_status s);
+
+/* Human-readable detail of the last error returned on this host thread
+ * (static thread-local buffer; empty after a successful call). */
+const char *rr_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RR_H */

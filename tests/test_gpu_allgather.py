@@ -1,0 +1,227 @@
+"""GPU parity: rank-major and param-contiguous allgather through the C ABI,
+bit for bit against the CPU oracle, on both copy engines (128-bit
+loads/stores and TMA bulk copies).  Random-bit inputs carry NaN and Inf
+encodings, which must survive untouched."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from gpu_util import GuardedOutputs, RankBuffers, assert_bitwise
+
+pytestmark = pytest.mark.gpu
+
+ENGINES = {"ldst": 1, "tma": 2}
+
+
+@pytest.fixture(scope="module")
+def rr():
+    if not torch.cuda.is_available():
+        pytest.fail("these tests need a CUDA GPU")
+    from allgather_rr_allreduce_gb300 import build
+    build.build()
+    import allgather_rr_allreduce_gb300 as m
+    m.lib()
+    return m
+
+
+_pads = {}
+
+
+def pad_for(rr, W):
+    if W not in _pads:
+        _pads[W] = rr.rr_signal_pad_create(W)
+    return _pads[W]
+
+
+def gather(rr, W, dtype, ins, splits=None, engine="tma", materialise=None, blocks_per_rank=0,
+           layout="packed"):
+    pad = pad_for(rr, W)
+    pad.set_option("gather_engine", ENGINES[engine])
+    pad.set_option("blocks_per_rank", blocks_per_rank)
+    n = ins[0].size
+    bufs = RankBuffers(W, n, dtype, layout=layout)
+    bufs.fill(ins)
+    outs = GuardedOutputs(W, W * n, dtype, materialise=materialise)
+    if splits is None:
+        rr.rr_allgather(bufs.ptrs, outs.ptrs, W, n, dtype, pad)
+    else:
+        rr.rr_allgather_param_contiguous(bufs.ptrs, outs.ptrs, W, splits, dtype, pad)
+    pad.status()
+    assert pad.get_option("last_engine") == ENGINES[engine]
+    pad.set_option("blocks_per_rank", 0)
+    return bufs, outs
+
+
+RM_SHAPES = [(2, 4096), (1, 17), (2, 3), (3, 1001), (8, 8192), (8, 4097), (5, 123_457), (16, 2048),
+             (8, 1)]
+
+
+@pytest.mark.parametrize("engine", list(ENGINES))
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32", "int32"])
+@pytest.mark.parametrize("W,N", RM_SHAPES, ids=[f"W{w}_N{n}" for w, n in RM_SHAPES])
+def test_rank_major_matches_oracle(rr, engine, dtype, W, N):
+    ins = workloads.rank_buffers(W, N, dtype, "bits", seed_base=40 * W + N % 89)
+    want = oracle.allgather_rank_major(ins, dtype)
+    bufs, outs = gather(rr, W, dtype, ins, engine=engine)
+    for q in range(W):
+        assert_bitwise(outs.host(q), want, f"output {q}")
+    outs.check_guards()
+    for r in range(W):
+        assert_bitwise(bufs.host(r), ins[r], f"shard {r} after the call")
+
+
+@pytest.mark.parametrize("engine", list(ENGINES))
+@pytest.mark.parametrize("materialise", [(0,), (2, 5), (7,)])
+def test_rank_major_subset_of_outputs(rr, engine, materialise):
+    W, N, dtype = 8, 300_000, "bf16"
+    ins = workloads.rank_buffers(W, N, dtype, "bits", seed_base=3)
+    want = oracle.allgather_rank_major(ins, dtype)
+    _, outs = gather(rr, W, dtype, ins, engine=engine, materialise=materialise)
+    for q in materialise:
+        assert_bitwise(outs.host(q), want, f"output {q}")
+    outs.check_guards()
+
+
+SPLIT_TABLES = {
+    "aligned": [4096, 512, 512, 4096, 8 * 2368, 8 * 2368, 8 * 2368],
+    "ragged": [5, 1, 0, 7, 2, 1023, 3],
+    "empty_ends": [0, 64, 0, 0, 33, 0],
+    "one": [77_777],
+    "many_small": [1 + (i * 7) % 13 for i in range(256)],
+}
+
+
+@pytest.mark.parametrize("engine", list(ENGINES))
+@pytest.mark.parametrize("dtype", ["bf16", "fp32", "int32", "fp16"])
+@pytest.mark.parametrize("table", list(SPLIT_TABLES))
+@pytest.mark.parametrize("W", [2, 3, 8])
+def test_param_contiguous_matches_oracle(rr, engine, dtype, table, W):
+    splits = SPLIT_TABLES[table]
+    ins = workloads.rank_buffers(W, sum(splits), dtype, "bits", seed_base=900 + W)
+    want = oracle.allgather_param_contiguous(ins, splits, dtype)
+    _, outs = gather(rr, W, dtype, ins, splits=splits, engine=engine)
+    for q in range(W):
+        assert_bitwise(outs.host(q), want, f"{table} output {q}")
+    outs.check_guards()
+
+
+@pytest.mark.parametrize("engine", list(ENGINES))
+@pytest.mark.parametrize("blocks", [1, 3, 100])
+def test_param_contiguous_fixed_blocks(rr, engine, blocks):
+    """One block per rank (the single-block degenerate case) and more blocks
+    than params: same bytes."""
+    W, splits, dtype = 4, [1000, 24, 4096, 8, 333], "bf16"
+    ins = workloads.rank_buffers(W, sum(splits), dtype, "bits", seed_base=5)
+    want = oracle.allgather_param_contiguous(ins, splits, dtype)
+    _, outs = gather(rr, W, dtype, ins, splits=splits, engine=engine, blocks_per_rank=blocks)
+    for q in range(W):
+        assert_bitwise(outs.host(q), want)
+
+
+@pytest.mark.parametrize("engine", list(ENGINES))
+def test_fsdp_layer_full(rr, engine):
+    """One transformer layer (hidden 3584 / kv 512 / ffn 18944), W=8, bf16,
+    N(0, 0.02): the whole output against the oracle and against the unsharded
+    weights themselves."""
+    cfg = workloads.FSDP_LAYER
+    W = cfg["W"]
+    full, shards = workloads.fsdp_layer_shards(W, layer=0, sigma=cfg["sigma"], seed_base=cfg["seed_base"])
+    splits = workloads.shard_sizes(workloads.FSDP_LAYER_PARAMS, W)
+    want = oracle.allgather_param_contiguous(shards, splits, "bf16")
+    assert np.array_equal(want, np.concatenate(full))
+    _, outs = gather(rr, W, "bf16", shards, splits=splits, engine=engine, materialise=(0, 5))
+    for q in (0, 5):
+        assert_bitwise(outs.host(q), want, f"output {q}")
+    outs.check_guards()
+
+
+def test_fsdp_28_layers_unshard_property(rr):
+    """28 layers back to back on distinct device buffers, as the benchmark
+    runs them.  Weights are drawn on the device; the check is the property
+    that holds at any size: the param-contiguous output of layer l equals
+    layer l's flattened weights concatenated in param order."""
+    cfg = workloads.FSDP_LAYER
+    W, L = cfg["W"], cfg["layers"]
+    splits = workloads.shard_sizes(workloads.FSDP_LAYER_PARAMS, W)
+    S = sum(splits)
+    pad = pad_for(rr, W)
+    pad.set_option("gather_engine", 0)
+    g = torch.Generator(device="cuda").manual_seed(cfg["seed_base"])
+    layers = []
+    for l in range(L):
+        weights = (torch.randn(W * S, generator=g, device="cuda") * cfg["sigma"]).to(torch.bfloat16)
+        shards = torch.empty((W, S), dtype=torch.bfloat16, device="cuda")
+        o = 0
+        for s, e in enumerate(splits):
+            shards[:, o:o + e] = weights[o * W:(o + e) * W].view(W, e)
+            o += e
+        out = torch.empty(W * S, dtype=torch.bfloat16, device="cuda")
+        layers.append((weights, shards, out))
+    for weights, shards, out in layers:
+        rr.rr_allgather_param_contiguous([shards[r] for r in range(W)], [out] + [None] * (W - 1), W,
+                                         splits, "bf16", pad)
+    pad.status()
+    for l, (weights, _, out) in enumerate(layers):
+        assert torch.equal(out.view(torch.int16), weights.view(torch.int16)), f"layer {l}"
+
+
+def _sweep_sizes():
+    return [1 << k for k in range(10, 30)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32", "int32"])
+def test_allgather_size_sweep(rr, dtype):
+    """W=8, 1 KiB .. 512 MiB per rank, random bits.  Up to 64 MiB per rank
+    the whole output is compared with the oracle on the host; above, on the
+    device, with the property every size obeys: output slice r is rank r's
+    shard (the output crosses 2^32 bytes at 512 MiB per rank)."""
+    W = 8
+    eb = workloads.ELEM_BYTES[dtype]
+    pad = pad_for(rr, W)
+    pad.set_option("gather_engine", 0)
+    for nbytes in _sweep_sizes():
+        n = nbytes // eb
+        if nbytes <= 64 << 20:
+            ins = workloads.rank_buffers(W, n, dtype, "bits", seed_base=4000 + nbytes % 1000)
+            want = oracle.allgather_rank_major(ins, dtype)
+            bufs = RankBuffers(W, n, dtype)
+            bufs.fill(ins)
+            outs = GuardedOutputs(W, W * n, dtype, materialise=(0,))
+            rr.rr_allgather(bufs.ptrs, outs.ptrs, W, n, dtype, pad)
+            pad.status()
+            assert_bitwise(outs.host(0), want, f"{nbytes} B per rank")
+            outs.check_guards()
+            del bufs, outs
+        else:
+            it = torch.int16 if eb == 2 else torch.int32
+            info = torch.iinfo(it)
+            gen = torch.Generator(device="cuda").manual_seed(nbytes)
+            shards = torch.randint(info.min, info.max, (W, n), dtype=it, device="cuda", generator=gen)
+            out = torch.empty(W * n, dtype=it, device="cuda")
+            rr.rr_allgather([shards[r] for r in range(W)], [out] + [None] * (W - 1), W, n, dtype, pad)
+            pad.status()
+            assert torch.equal(out.view(W, n), shards), f"{nbytes} B per rank"
+            del shards, out
+            torch.cuda.empty_cache()
+
+
+def test_gather_argument_errors(rr):
+    W, N = 4, 1024
+    pad = pad_for(rr, W)
+    bufs = RankBuffers(W, N, "fp32")
+    outs = GuardedOutputs(W, W * N, "fp32")
+    with pytest.raises(rr.RRError) as e:
+        rr.rr_allgather(bufs.ptrs, [bufs.ptrs[1] - 16, None, None, None], W, N, "fp32", pad)
+    assert e.value.status == rr.RR_ERR_ALIAS
+    with pytest.raises(rr.RRError) as e:
+        rr.rr_allgather_param_contiguous(bufs.ptrs, outs.ptrs, W, [10, -1], "fp32", pad)
+    assert e.value.status == rr.RR_ERR_INVALID_ARG
+    with pytest.raises(rr.RRError) as e:
+        rr.rr_allgather_param_contiguous(bufs.ptrs, outs.ptrs, W, [1] * 257, "fp32", pad)
+    assert e.value.status == rr.RR_ERR_INVALID_ARG
+    with pytest.raises(rr.RRError) as e:
+        rr.rr_allgather(bufs.ptrs, [outs.ptrs[0] + 4, None, None, None], W, N, "fp32", pad)
+    assert e.value.status == rr.RR_ERR_ALIGNMENT
+    pad.status()
