@@ -1,0 +1,552 @@
+"""Benchmark of the reduce/gather hot path on one GB300 (W ranks emulated in
+its HBM), printing one JSON line.
+
+A step is one pass of the whole hot path over the large workload (W=8, bf16,
+2^24 elements = 32 MiB per rank, N(0,1)), one launch per op:
+  oneshot_copy_off   one-shot allreduce, registered buffers, rank 0's output
+  oneshot_copy_on    one-shot allreduce, inputs staged in-kernel, rank 0's output
+  twoshot_copy_off   two-shot allreduce, all W outputs
+  twoshot_copy_on    two-shot allreduce with in-kernel staging, all W outputs
+  allgather          rank-major all_gather_into_tensor, rank 0's output
+  allgather_pc       param-contiguous (FSDP) allgather of one transformer layer
+                     (hidden 3584 / kv 512 / ffn 18944, W=8), rank 0's output
+value = algorithmic bytes of the step / device time of the step (GB/s).
+Algorithmic bytes of an op = every byte that exists before the call and must
+be read once, plus every byte written (re-reads of data written earlier in
+the same call are not counted).  Each op has its own buffers (>= 288 MiB per
+op, more than the 129 MB L2), so no op starts with its inputs in L2.
+
+--impl reference times the CPU oracle (the plain definition of every op) on
+the host on a sample of the same workload and reports the same metric.
+Under torchrun each rank runs an independent replica (the path does not
+shard over GPUs); the time is the max over ranks.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "achieved HBM GB/s and % of 8 TB/s roofline per op vs bytes/rank; small-msg µs"
+NOMINAL_HBM_GBS = 8000.0
+W, N = workloads.LARGE["W"], workloads.LARGE["N"]
+EB = 2
+OP_NAMES = ("oneshot_copy_off", "oneshot_copy_on", "twoshot_copy_off", "twoshot_copy_on",
+            "allgather", "allgather_pc")
+
+
+def op_bytes(pc_shard_bytes):
+    """Algorithmic bytes of each op of the step."""
+    nb = N * EB
+    return {
+        "oneshot_copy_off": W * nb + nb,            # read W buffers, write rank 0's output
+        "oneshot_copy_on": W * nb + W * nb + nb,    # + stage W inputs into the registered buffers
+        "twoshot_copy_off": W * nb + W * nb,        # read W buffers, write W outputs
+        "twoshot_copy_on": W * nb + W * nb + W * nb,
+        "allgather": W * nb + W * nb,               # read W shards, write one W*N output
+        "allgather_pc": 2 * W * pc_shard_bytes,
+    }
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "allgather_rr_allreduce_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_op):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("csrc_sha256_16") != source_hash():
+        return None
+    ent = d.get("ops", {}).get(kernel_op)
+    return None if ent is None else ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons every 50 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sms, maxes, reasons = [], [], set()
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sms.append(float(f[1]))
+                maxes.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                  "sw_power_cap"), f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "samples": len(sms),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------- GPU arm
+
+class Step:
+    """Device buffers and pre-marshalled C calls of one step."""
+
+    def __init__(self, rr, stream, seed):
+        self.rr = rr
+        self.stream = stream
+        dev = "cuda"
+        g = torch.Generator(device=dev).manual_seed(seed)
+        nb = N
+
+        def ranks():
+            return (torch.randn((W, nb), generator=g, device=dev)).to(torch.bfloat16)
+
+        self.pad = rr.rr_signal_pad_create(W)
+        sh = stream.cuda_stream
+        bf16 = rr.RR_BF16
+        # one-shot, registered buffers
+        self.os_off_in = ranks()
+        self.os_off_out = torch.empty(nb, dtype=torch.bfloat16, device=dev)
+        # one-shot, staged
+        self.os_on_in = ranks()
+        self.os_on_reg = torch.empty((W, nb), dtype=torch.bfloat16, device=dev)
+        self.os_on_out = torch.empty(nb, dtype=torch.bfloat16, device=dev)
+        # two-shot
+        self.ts_off_in = ranks()
+        self.ts_off_out = torch.empty((W, nb), dtype=torch.bfloat16, device=dev)
+        self.ts_on_in = ranks()
+        self.ts_on_reg = torch.empty((W, nb), dtype=torch.bfloat16, device=dev)
+        self.ts_on_out = torch.empty((W, nb), dtype=torch.bfloat16, device=dev)
+        # rank-major allgather
+        self.ag_in = ranks()
+        self.ag_out = torch.empty(W * nb, dtype=torch.bfloat16, device=dev)
+        # param-contiguous allgather of one layer
+        self.splits = workloads.shard_sizes(workloads.FSDP_LAYER_PARAMS, W)
+        S = sum(self.splits)
+        self.pc_in = (torch.randn((W, S), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        self.pc_out = torch.empty(W * S, dtype=torch.bfloat16, device=dev)
+        self.pc_shard_bytes = S * EB
+
+        def rows(t):
+            return [t[r].data_ptr() for r in range(W)]
+
+        def only0(t):
+            return [t.data_ptr()] + [None] * (W - 1)
+
+        import ctypes
+        sp = (ctypes.c_int64 * len(self.splits))(*self.splits)
+        self._keep = sp
+        bc = rr.bound_call
+        self.calls = {
+            "oneshot_copy_off": bc("rr_allreduce_oneshot", None, rows(self.os_off_in), only0(self.os_off_out),
+                                   W, nb, bf16, 0, self.pad, sh),
+            "oneshot_copy_on": bc("rr_allreduce_oneshot", rows(self.os_on_in), rows(self.os_on_reg),
+                                  only0(self.os_on_out), W, nb, bf16, 1, self.pad, sh),
+            "twoshot_copy_off": bc("rr_allreduce_twoshot", None, rows(self.ts_off_in), rows(self.ts_off_out),
+                                   W, nb, bf16, 0, self.pad, sh),
+            "twoshot_copy_on": bc("rr_allreduce_twoshot", rows(self.ts_on_in), rows(self.ts_on_reg),
+                                  rows(self.ts_on_out), W, nb, bf16, 1, self.pad, sh),
+            "allgather": bc("rr_allgather", rows(self.ag_in), only0(self.ag_out), W, nb, bf16, self.pad, sh),
+            "allgather_pc": bc("rr_allgather_param_contiguous", rows(self.pc_in), only0(self.pc_out), W, sp,
+                               len(self.splits), bf16, self.pad, sh),
+        }
+        # host-side copies for the end-to-end measurement
+        self.e2e_pairs_in = [(t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True))
+                             for t in (self.os_off_in, self.os_on_in, self.ts_off_in, self.ts_on_in,
+                                       self.ag_in, self.pc_in)]
+        for d, h in self.e2e_pairs_in:
+            h.copy_(d)
+        self.e2e_pairs_out = [(t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True))
+                              for t in (self.os_off_out, self.os_on_out, self.ts_off_out, self.ts_on_out,
+                                        self.ag_out, self.pc_out)]
+
+    def run(self, events=None):
+        for i, name in enumerate(OP_NAMES):
+            if events is not None:
+                events[i][0].record(self.stream)
+            self.calls[name]()
+            if events is not None:
+                events[i][1].record(self.stream)
+
+    def run_e2e(self):
+        for d, h in self.e2e_pairs_in:
+            d.copy_(h, non_blocking=True)
+        self.run()
+        for d, h in self.e2e_pairs_out:
+            h.copy_(d, non_blocking=True)
+
+    def e2e_bytes(self):
+        bi = sum(h.numel() * h.element_size() for _, h in self.e2e_pairs_in)
+        bo = sum(h.numel() * h.element_size() for _, h in self.e2e_pairs_out)
+        return bi, bo
+
+
+def latency_sweep(rr, stream, reps=1000, batch=250):
+    """Small messages, W=8, bf16, one-shot and two-shot, all W outputs, `reps`
+    back-to-back calls on one pad.  Calls are queued behind a sleep kernel so
+    the events time the GPU executing them back to back (not host issue)."""
+    pad = rr.rr_signal_pad_create(W)
+    sh = stream.cuda_stream
+    out = {"oneshot": {}, "twoshot": {}, "issue_bound_oneshot": {}}
+    g = torch.Generator(device="cuda").manual_seed(workloads.LATENCY["seed_base"])
+    for nbytes in workloads.LATENCY["bytes_per_rank"]:
+        n = nbytes // EB
+        x = (torch.rand((W, n), generator=g, device="cuda") * 2 - 1).to(torch.bfloat16)
+        y = torch.empty((W, n), dtype=torch.bfloat16, device="cuda")
+        rows_x = [x[r].data_ptr() for r in range(W)]
+        rows_y = [y[r].data_ptr() for r in range(W)]
+        for algo in ("oneshot", "twoshot"):
+            call = rr.bound_call(f"rr_allreduce_{algo}", None, rows_x, rows_y, W, n, rr.RR_BF16, 0, pad, sh)
+            for _ in range(20):
+                call()
+            total_ms = 0.0
+            with torch.cuda.stream(stream):
+                for _ in range(reps // batch):
+                    torch.cuda._sleep(20_000_000)
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    for _ in range(batch):
+                        call()
+                    e1.record(stream)
+                    e1.synchronize()
+                    total_ms += e0.elapsed_time(e1)
+            out[algo][str(nbytes)] = round(1000.0 * total_ms / reps, 3)
+            if algo == "oneshot":
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                stream.synchronize()
+                e0.record(stream)
+                for _ in range(reps):
+                    call()
+                e1.record(stream)
+                e1.synchronize()
+                out["issue_bound_oneshot"][str(nbytes)] = round(1000.0 * e0.elapsed_time(e1) / reps, 3)
+    pad.status(stream)
+    pad.close()
+    return out
+
+
+def fsdp_28_layers(rr, stream):
+    """28 param-contiguous allgathers back to back, one per layer, on distinct
+    buffers (about 13 GB in, 13 GB out), rank 0's output."""
+    cfg = workloads.FSDP_LAYER
+    splits = workloads.shard_sizes(workloads.FSDP_LAYER_PARAMS, W)
+    S = sum(splits)
+    pad = rr.rr_signal_pad_create(W)
+    g = torch.Generator(device="cuda").manual_seed(cfg["seed_base"])
+    import ctypes
+    sp = (ctypes.c_int64 * len(splits))(*splits)
+    calls, keep = [], []
+    for _ in range(cfg["layers"]):
+        x = (torch.randn((W, S), generator=g, device="cuda") * cfg["sigma"]).to(torch.bfloat16)
+        y = torch.empty(W * S, dtype=torch.bfloat16, device="cuda")
+        keep.append((x, y))
+        calls.append(rr.bound_call("rr_allgather_param_contiguous", [x[r].data_ptr() for r in range(W)],
+                                   [y.data_ptr()] + [None] * (W - 1), W, sp, len(splits), rr.RR_BF16,
+                                   pad, stream.cuda_stream))
+    times = []
+    for rep in range(4):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for c in calls:
+            c()
+        e1.record(stream)
+        e1.synchronize()
+        if rep:
+            times.append(e0.elapsed_time(e1))
+    pad.status(stream)
+    pad.close()
+    ms = min(times)
+    total = cfg["layers"] * 2 * W * S * EB
+    return {"ms": round(ms, 4), "GBps": round(total / ms / 1e6, 1), "bytes": total,
+            "pct_of_8TBps": round(100 * total / ms / 1e6 / NOMINAL_HBM_GBS, 2)}
+
+
+def run_gpu(args, rank, world, local_rank):
+    import allgather_rr_allreduce_gb300 as rr
+    from allgather_rr_allreduce_gb300 import build as rr_build
+    rr_build.build()
+    torch.cuda.set_device(local_rank)
+    stream = torch.cuda.Stream()
+    step = Step(rr, stream, seed=workloads.LARGE["seed_base"] + 97 * rank)
+    bytes_by_op = op_bytes(step.pc_shard_bytes)
+    step_bytes = sum(bytes_by_op.values())
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank)
+    if rank == 0:
+        sampler.start()
+    for _ in range(args.warmup):
+        step.run()
+    stream.synchronize()
+
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in OP_NAMES]
+              for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for k in range(args.steps):
+        step.run(events[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if rank == 0 else None
+    step.pad.status(stream)
+    elapsed_ms = t_start.elapsed_time(t_end)
+    per_op_ms = {name: [events[k][i][0].elapsed_time(events[k][i][1]) for k in range(args.steps)]
+                 for i, name in enumerate(OP_NAMES)}
+
+    max_ms = elapsed_ms
+    if world > 1:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        max_ms = float(t.item())
+
+    # end to end through the public API: host inputs in, host outputs out
+    e2e_steps = max(1, min(args.steps, 5))
+    with torch.cuda.stream(stream):
+        step.run_e2e()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            step.run_e2e()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    bi, bo = step.e2e_bytes()
+
+    if rank != 0:
+        return None
+
+    peak, peak_kind = measured_peaks()
+    ops = {}
+    for name in OP_NAMES:
+        ms = statistics.mean(per_op_ms[name])
+        gbs = bytes_by_op[name] / ms / 1e6
+        ops[name] = {"bytes": bytes_by_op[name], "us": round(1000 * ms, 2),
+                     "us_median": round(1000 * statistics.median(per_op_ms[name]), 2),
+                     "GBps": round(gbs, 1), "pct_of_8TBps": round(100 * gbs / NOMINAL_HBM_GBS, 2),
+                     f"frac_of_{peak_kind}": round(gbs / peak, 4)}
+    dominant = max(OP_NAMES, key=lambda n: ops[n]["us"])
+    dom = ops[dominant]
+    ms_per_step = max_ms / args.steps
+    value = world * step_bytes / ms_per_step / 1e6
+
+    extras = {}
+    if not args.no_extras:
+        extras["latency_us"] = latency_sweep(rr, stream)
+        extras["fsdp_28_layers"] = fsdp_28_layers(rr, stream)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded torch RNG on the device; N(0,1) ranks, N(0,0.02) layer shards)",
+        "config": {"workload": "W8_bf16_2^24 (32 MiB/rank): oneshot+twoshot x copy_mode off/on, "
+                               "rank-major allgather; one FSDP layer (hidden 3584/kv 512/ffn 18944) "
+                               "param-contiguous allgather",
+                   "W": W, "numel_per_rank": N, "bytes_per_step": step_bytes,
+                   "l2": "inputs larger than L2 (every op >= 288 MiB of its own buffers; L2 129 MB)",
+                   "parallelism": f"replicas x{world} (no inter-GPU collective; W ranks emulated per GPU)"},
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": dom["GBps"], "peak": peak,
+                     "peak_kind": f"{peak_kind} hbm_gbs (STREAM-style copy, burst)", "unit": "GB/s",
+                     "frac": round(dom["GBps"] / peak, 4), "traffic": recorded_traffic(dominant),
+                     "algorithmic_bytes_per_launch": bytes_by_op[dominant]},
+        "ops": ops,
+        "e2e": {"value": round(world * step_bytes / e2e_ms / 1e6, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
+        "gpu_launches": len(OP_NAMES) * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": None,
+    }
+    line.update(extras)
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(sample_div=1, reps=3)
+    return line
+
+
+# ---------------------------------------------------------------------- CPU arm
+
+def _cpu_workload(sample_div, seed):
+    n = N // sample_div
+    splits = [e // sample_div for e in workloads.shard_sizes(workloads.FSDP_LAYER_PARAMS, W)]
+    ins = {k: workloads.rank_buffers(W, n, "bf16", "normal", seed_base=seed + 10 * i)
+           for i, k in enumerate(("os_off", "os_on", "ts_off", "ts_on", "ag"))}
+    ins["pc"] = workloads.rank_buffers(W, sum(splits), "bf16", "normal", seed_base=seed + 99, sigma=0.02)
+    return n, splits, ins
+
+
+def _cpu_step(oracle, n, splits, ins):
+    # The oracle's definition of each op.  Staging (copy_mode) is a copy of
+    # each input into its registered buffer, then the same sum.
+    oracle.allreduce(ins["os_off"], "bf16")
+    staged = [np.array(a, copy=True) for a in ins["os_on"]]
+    oracle.allreduce(staged, "bf16")
+    oracle.allreduce(ins["ts_off"], "bf16")
+    staged = [np.array(a, copy=True) for a in ins["ts_on"]]
+    oracle.allreduce(staged, "bf16")
+    oracle.allgather_rank_major(ins["ag"], "bf16")
+    oracle.allgather_param_contiguous(ins["pc"], splits, "bf16")
+
+
+def _cpu_bytes(n, splits):
+    nb = n * EB
+    pc = sum(splits) * EB
+    # same accounting as the GPU arm; two-shot outputs counted for all W ranks
+    # (the oracle writes one vector; the other W-1 are identical copies).
+    return (W * nb + nb) + (2 * W * nb + nb) + 2 * W * nb + 3 * W * nb + 2 * W * nb + 2 * W * pc
+
+
+def cpu_baseline(sample_div=8, reps=1):
+    import oracle
+    oracle.lib()
+    n, splits, ins = _cpu_workload(sample_div, seed=7000)
+    _cpu_step(oracle, n, splits, ins)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        _cpu_step(oracle, n, splits, ins)
+    dt = (time.perf_counter() - t0) / reps
+    b = _cpu_bytes(n, splits)
+    return {"value": round(b / dt / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"one full step at 1/{sample_div} of every op's elements per rank "
+                      f"({n} elements per rank, layer splits / {sample_div}), {reps} rep(s), "
+                      f"{dt:.2f} s per step, single-threaded C"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.lib()
+    sample_div = 16
+    n, splits, ins = _cpu_workload(sample_div, seed=8000)
+    for _ in range(args.warmup):
+        _cpu_step(oracle, n, splits, ins)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _cpu_step(oracle, n, splits, ins)
+    dt = (time.perf_counter() - t0) / args.steps
+    b = _cpu_bytes(n, splits)
+    v = b / dt / 1e9
+    sample = (f"each step: the whole hot path at 1/{sample_div} of every op's elements per rank "
+              f"({n} bf16 per rank, layer splits / {sample_div}); single-threaded C oracle")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * dt, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; N(0,1) ranks, N(0,0.02) layer shards)",
+        "config": {"workload": f"W8_bf16_2^24 hot path, sampled at 1/{sample_div}", "W": W,
+                   "numel_per_rank": n, "parallelism": "CPU oracle, rank 0 only"},
+        "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("rr", "reference"), default="rr")
+    ap.add_argument("--no-extras", action="store_true", help="skip the latency sweep and the 28-layer run")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            torch.cuda.set_device(local_rank)
+            torch.distributed.init_process_group("nccl")
+        line = run_gpu(args, rank, world, local_rank)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
