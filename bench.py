@@ -46,19 +46,6 @@ OP_NAMES = ("oneshot_copy_off", "oneshot_copy_on", "twoshot_copy_off", "twoshot_
             "allgather", "allgather_pc")
 
 
-def op_bytes(pc_shard_bytes):
-    """Algorithmic bytes of each op of the step."""
-    nb = N * EB
-    return {
-        "oneshot_copy_off": W * nb + nb,            # read W buffers, write rank 0's output
-        "oneshot_copy_on": W * nb + W * nb + nb,    # + stage W inputs into the registered buffers
-        "twoshot_copy_off": W * nb + W * nb,        # read W buffers, write W outputs
-        "twoshot_copy_on": W * nb + W * nb + W * nb,
-        "allgather": W * nb + W * nb,               # read W shards, write one W*N output
-        "allgather_pc": 2 * W * pc_shard_bytes,
-    }
-
-
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -143,43 +130,24 @@ class ClockSampler:
 # ---------------------------------------------------------------------- GPU arm
 
 class Step:
-    """Device buffers and pre-marshalled C calls of one step."""
+    """Device buffers and pre-marshalled C calls of one step (all ops, or the
+    subset `ops`; `n` elements per rank for the allreduce / allgather ops and
+    the FSDP layer's splits divided by `pc_div`)."""
 
-    def __init__(self, rr, stream, seed):
+    def __init__(self, rr, stream, seed, ops=OP_NAMES, n=N, pc_div=1):
+        import ctypes
         self.rr = rr
         self.stream = stream
+        self.ops = tuple(ops)
+        self.n = n
         dev = "cuda"
         g = torch.Generator(device=dev).manual_seed(seed)
-        nb = N
 
         def ranks():
-            return (torch.randn((W, nb), generator=g, device=dev)).to(torch.bfloat16)
+            return torch.randn((W, n), generator=g, device=dev).to(torch.bfloat16)
 
-        self.pad = rr.rr_signal_pad_create(W)
-        sh = stream.cuda_stream
-        bf16 = rr.RR_BF16
-        # one-shot, registered buffers
-        self.os_off_in = ranks()
-        self.os_off_out = torch.empty(nb, dtype=torch.bfloat16, device=dev)
-        # one-shot, staged
-        self.os_on_in = ranks()
-        self.os_on_reg = torch.empty((W, nb), dtype=torch.bfloat16, device=dev)
-        self.os_on_out = torch.empty(nb, dtype=torch.bfloat16, device=dev)
-        # two-shot
-        self.ts_off_in = ranks()
-        self.ts_off_out = torch.empty((W, nb), dtype=torch.bfloat16, device=dev)
-        self.ts_on_in = ranks()
-        self.ts_on_reg = torch.empty((W, nb), dtype=torch.bfloat16, device=dev)
-        self.ts_on_out = torch.empty((W, nb), dtype=torch.bfloat16, device=dev)
-        # rank-major allgather
-        self.ag_in = ranks()
-        self.ag_out = torch.empty(W * nb, dtype=torch.bfloat16, device=dev)
-        # param-contiguous allgather of one layer
-        self.splits = workloads.shard_sizes(workloads.FSDP_LAYER_PARAMS, W)
-        S = sum(self.splits)
-        self.pc_in = (torch.randn((W, S), generator=g, device=dev) * 0.02).to(torch.bfloat16)
-        self.pc_out = torch.empty(W * S, dtype=torch.bfloat16, device=dev)
-        self.pc_shard_bytes = S * EB
+        def empty(*shape):
+            return torch.empty(shape, dtype=torch.bfloat16, device=dev)
 
         def rows(t):
             return [t[r].data_ptr() for r in range(W)]
@@ -187,35 +155,63 @@ class Step:
         def only0(t):
             return [t.data_ptr()] + [None] * (W - 1)
 
-        import ctypes
-        sp = (ctypes.c_int64 * len(self.splits))(*self.splits)
-        self._keep = sp
+        self.pad = rr.rr_signal_pad_create(W)
+        sh = stream.cuda_stream
+        bf16 = rr.RR_BF16
         bc = rr.bound_call
-        self.calls = {
-            "oneshot_copy_off": bc("rr_allreduce_oneshot", None, rows(self.os_off_in), only0(self.os_off_out),
-                                   W, nb, bf16, 0, self.pad, sh),
-            "oneshot_copy_on": bc("rr_allreduce_oneshot", rows(self.os_on_in), rows(self.os_on_reg),
-                                  only0(self.os_on_out), W, nb, bf16, 1, self.pad, sh),
-            "twoshot_copy_off": bc("rr_allreduce_twoshot", None, rows(self.ts_off_in), rows(self.ts_off_out),
-                                   W, nb, bf16, 0, self.pad, sh),
-            "twoshot_copy_on": bc("rr_allreduce_twoshot", rows(self.ts_on_in), rows(self.ts_on_reg),
-                                  rows(self.ts_on_out), W, nb, bf16, 1, self.pad, sh),
-            "allgather": bc("rr_allgather", rows(self.ag_in), only0(self.ag_out), W, nb, bf16, self.pad, sh),
-            "allgather_pc": bc("rr_allgather_param_contiguous", rows(self.pc_in), only0(self.pc_out), W, sp,
-                               len(self.splits), bf16, self.pad, sh),
-        }
+        self.splits = [e // pc_div for e in workloads.shard_sizes(workloads.FSDP_LAYER_PARAMS, W)]
+        S = sum(self.splits)
+        self.pc_shard_bytes = S * EB
+        self._sp = (ctypes.c_int64 * len(self.splits))(*self.splits)
+        self.calls, ins, outs = {}, [], []
+        for op in self.ops:
+            if op == "oneshot_copy_off":
+                x, y = ranks(), empty(n)
+                self.calls[op] = bc("rr_allreduce_oneshot", None, rows(x), only0(y), W, n, bf16, 0, self.pad, sh)
+            elif op == "oneshot_copy_on":
+                x, reg, y = ranks(), empty(W, n), empty(n)
+                self.calls[op] = bc("rr_allreduce_oneshot", rows(x), rows(reg), only0(y), W, n, bf16, 1,
+                                    self.pad, sh)
+            elif op == "twoshot_copy_off":
+                x, y = ranks(), empty(W, n)
+                self.calls[op] = bc("rr_allreduce_twoshot", None, rows(x), rows(y), W, n, bf16, 0, self.pad, sh)
+            elif op == "twoshot_copy_on":
+                x, reg, y = ranks(), empty(W, n), empty(W, n)
+                self.calls[op] = bc("rr_allreduce_twoshot", rows(x), rows(reg), rows(y), W, n, bf16, 1,
+                                    self.pad, sh)
+            elif op == "allgather":
+                x, y = ranks(), empty(W * n)
+                self.calls[op] = bc("rr_allgather", rows(x), only0(y), W, n, bf16, self.pad, sh)
+            elif op == "allgather_pc":
+                x = (torch.randn((W, S), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+                y = empty(W * S)
+                self.calls[op] = bc("rr_allgather_param_contiguous", rows(x), only0(y), W, self._sp,
+                                    len(self.splits), bf16, self.pad, sh)
+            else:
+                raise ValueError(f"unknown op {op}")
+            ins.append(x)
+            outs.append(y)
+        self._bufs = (ins, outs)
         # host-side copies for the end-to-end measurement
-        self.e2e_pairs_in = [(t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True))
-                             for t in (self.os_off_in, self.os_on_in, self.ts_off_in, self.ts_on_in,
-                                       self.ag_in, self.pc_in)]
+        self.e2e_pairs_in = [(t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)) for t in ins]
         for d, h in self.e2e_pairs_in:
             h.copy_(d)
-        self.e2e_pairs_out = [(t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True))
-                              for t in (self.os_off_out, self.os_on_out, self.ts_off_out, self.ts_on_out,
-                                        self.ag_out, self.pc_out)]
+        self.e2e_pairs_out = [(t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)) for t in outs]
+
+    def bytes_by_op(self):
+        nb = self.n * EB
+        full = {
+            "oneshot_copy_off": W * nb + nb,            # read W buffers, write rank 0's output
+            "oneshot_copy_on": W * nb + W * nb + nb,    # + stage W inputs into the registered buffers
+            "twoshot_copy_off": W * nb + W * nb,        # read W buffers, write W outputs
+            "twoshot_copy_on": W * nb + W * nb + W * nb,
+            "allgather": W * nb + W * nb,               # read W shards, write one W*N output
+            "allgather_pc": 2 * W * self.pc_shard_bytes,
+        }
+        return {op: full[op] for op in self.ops}
 
     def run(self, events=None):
-        for i, name in enumerate(OP_NAMES):
+        for i, name in enumerate(self.ops):
             if events is not None:
                 events[i][0].record(self.stream)
             self.calls[name]()
@@ -324,8 +320,10 @@ def run_gpu(args, rank, world, local_rank):
     rr_build.build()
     torch.cuda.set_device(local_rank)
     stream = torch.cuda.Stream()
-    step = Step(rr, stream, seed=workloads.LARGE["seed_base"] + 97 * rank)
-    bytes_by_op = op_bytes(step.pc_shard_bytes)
+    ops = tuple(args.only.split(",")) if args.only else OP_NAMES
+    step = Step(rr, stream, seed=workloads.LARGE["seed_base"] + 97 * rank, ops=ops,
+                n=args.numel or N, pc_div=args.pc_div)
+    bytes_by_op = step.bytes_by_op()
     step_bytes = sum(bytes_by_op.values())
     torch.cuda.synchronize()
 
@@ -336,7 +334,7 @@ def run_gpu(args, rank, world, local_rank):
         step.run()
     stream.synchronize()
 
-    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in OP_NAMES]
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in ops]
               for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -354,7 +352,7 @@ def run_gpu(args, rank, world, local_rank):
     step.pad.status(stream)
     elapsed_ms = t_start.elapsed_time(t_end)
     per_op_ms = {name: [events[k][i][0].elapsed_time(events[k][i][1]) for k in range(args.steps)]
-                 for i, name in enumerate(OP_NAMES)}
+                 for i, name in enumerate(ops)}
 
     max_ms = elapsed_ms
     if world > 1:
@@ -388,16 +386,17 @@ def run_gpu(args, rank, world, local_rank):
         return None
 
     peak, peak_kind = measured_peaks()
-    ops = {}
-    for name in OP_NAMES:
+    op_stats = {}
+    for name in ops:
         ms = statistics.mean(per_op_ms[name])
         gbs = bytes_by_op[name] / ms / 1e6
-        ops[name] = {"bytes": bytes_by_op[name], "us": round(1000 * ms, 2),
+        op_stats[name] = {"bytes": bytes_by_op[name], "us": round(1000 * ms, 2),
                      "us_median": round(1000 * statistics.median(per_op_ms[name]), 2),
                      "GBps": round(gbs, 1), "pct_of_8TBps": round(100 * gbs / NOMINAL_HBM_GBS, 2),
                      f"frac_of_{peak_kind}": round(gbs / peak, 4)}
-    dominant = max(OP_NAMES, key=lambda n: ops[n]["us"])
-    dom = ops[dominant]
+    dominant = max(ops, key=lambda n: op_stats[n]["us"])
+    step_bytes = sum(bytes_by_op.values())
+    dom = op_stats[dominant]
     ms_per_step = max_ms / args.steps
     value = world * step_bytes / ms_per_step / 1e6
 
@@ -419,20 +418,18 @@ def run_gpu(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded torch RNG on the device; N(0,1) ranks, N(0,0.02) layer shards)",
-        "config": {"workload": "W8_bf16_2^24 (32 MiB/rank): oneshot+twoshot x copy_mode off/on, "
-                               "rank-major allgather; one FSDP layer (hidden 3584/kv 512/ffn 18944) "
-                               "param-contiguous allgather",
-                   "W": W, "numel_per_rank": N, "bytes_per_step": step_bytes,
+        "config": {"workload": workload_name(ops, step.n, args.pc_div),
+                   "W": W, "numel_per_rank": step.n, "bytes_per_step": step_bytes,
                    "l2": "inputs larger than L2 (every op >= 288 MiB of its own buffers; L2 129 MB)",
                    "parallelism": f"replicas x{world} (no inter-GPU collective; W ranks emulated per GPU)"},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": dom["GBps"], "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs (STREAM-style copy, burst)", "unit": "GB/s",
                      "frac": round(dom["GBps"] / peak, 4), "traffic": recorded_traffic(dominant),
                      "algorithmic_bytes_per_launch": bytes_by_op[dominant]},
-        "ops": ops,
+        "ops": op_stats,
         "e2e": {"value": round(world * step_bytes / e2e_ms / 1e6, 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
-        "gpu_launches": len(OP_NAMES) * args.steps,
+        "gpu_launches": len(ops) * args.steps,
         "clocks": clocks,
         "cpu_baseline": None,
     }
@@ -440,6 +437,13 @@ def run_gpu(args, rank, world, local_rank):
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(sample_div=1, reps=3)
     return line
+
+
+def workload_name(ops, n, pc_div):
+    if tuple(ops) == OP_NAMES and n == N and pc_div == 1:
+        return ("W8_bf16_2^24 (32 MiB/rank): oneshot+twoshot x copy_mode off/on, rank-major allgather; "
+                "one FSDP layer (hidden 3584/kv 512/ffn 18944) param-contiguous allgather")
+    return f"subset {','.join(ops)} at W=8, {n} bf16 per rank, layer splits / {pc_div} (not the full step)"
 
 
 # ---------------------------------------------------------------------- CPU arm
@@ -529,6 +533,9 @@ def main():
     ap.add_argument("--impl", choices=("rr", "reference"), default="rr")
     ap.add_argument("--no-extras", action="store_true", help="skip the latency sweep and the 28-layer run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="", help="comma-separated subset of ops (profiling runs)")
+    ap.add_argument("--numel", type=int, default=0, help="elements per rank for the allreduce/allgather ops")
+    ap.add_argument("--pc-div", type=int, default=1, help="divide the FSDP layer's splits by this")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -102,8 +102,8 @@ typedef struct rr_signal_pad rr_signal_pad; /* opaque, owned by the library */
  * emits.  Layout here: [W listener][4 barriers][2 parities][blocks][W emitter]
  * uint32 words on the current device, plus a status block.  Each call takes
  * the next generation value g (a host counter, never 0) and writes g into
- * slots of parity g & 1, so consecutive calls never share a slot
- * ("offset = (flag % 2) ? world_size : 0" in the same post).
+ * slots of parity g & 1, so consecutive calls never share a slot (the same
+ * post picks the half of the arrival flags to use from the flag's parity).
  *
  * world_size: W, 1..RR_MAX_WORLD.  max_blocks_per_rank: upper bound on
  * blocks per rank any call on this pad may use (0 = 1024).  timeout_ns:
