@@ -525,3 +525,154 @@ const char *rr_status_string(rr_status s)
 const char *rr_last_error(void) { return g_err; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- no-alloc one-shot
+// rr_allreduce_oneshot_noalloc: the one-shot allreduce for callers that may
+// not allocate device memory.  Its signal pad lives in the fixed array below
+// instead of memory from rr_signal_pad_create; everything else is the one-shot
+// kernel above, unchanged.
+namespace {
+
+constexpr int kNoAllocMaxWorld = 8;    // largest W the fixed pad can serve
+constexpr int kNoAllocMaxBlocks = 32;  // largest blocks per rank it can serve
+constexpr size_t kNoAllocFlagWords =
+    (size_t)kNoAllocMaxWorld * kNoAllocMaxWorld * rr::kNumBarriers * 2 * kNoAllocMaxBlocks;
+
+struct NoAllocDevice {
+    uint32_t *scratch;  // device address of noalloc_scratch on this device
+    uint32_t gen;       // generation of the last call on this device
+};
+std::mutex g_noalloc_mu;
+std::map<int, NoAllocDevice> g_noalloc;
+
+}  // namespace
+
+// Flags ([W][4 barriers][2 parities][32 blocks][W] for the call's W) followed
+// by the status words: 64 KiB + 32 B, zero at module load, on every device
+// that loads this library, held until the process exits.
+static __device__ __align__(256) uint32_t noalloc_scratch[kNoAllocFlagWords + rr::kStatusWords];
+
+extern "C" rr_status rr_allreduce_oneshot_noalloc(const void *const *inputs, void *const *rank_bufs,
+                                                  void *const *outputs, int world_size, int64_t numel,
+                                                  rr_dtype dtype, int copy_mode, cudaStream_t stream)
+{
+    const int W = world_size;
+    if (W < 1 || W > kNoAllocMaxWorld)
+        return fail(RR_ERR_INVALID_ARG,
+                    "world_size %d: the allocation-free one-shot serves 1..%d ranks (its fixed signal pad "
+                    "holds %d x %d ranks x %d blocks per rank); use rr_allreduce_oneshot with a pad",
+                    W, kNoAllocMaxWorld, kNoAllocMaxWorld, kNoAllocMaxWorld, kNoAllocMaxBlocks);
+    const int eb = elem_bytes(dtype);
+    if (eb == 0) return fail(RR_ERR_UNSUPPORTED_DTYPE, "dtype %d", (int)dtype);
+    if (numel < 0 || numel > ((int64_t)1 << 40)) return fail(RR_ERR_INVALID_ARG, "numel %lld", (long long)numel);
+    if (!rank_bufs || !outputs) return fail(RR_ERR_INVALID_ARG, "rank_bufs / outputs array is NULL");
+    if (copy_mode && !inputs) return fail(RR_ERR_INVALID_ARG, "copy_mode needs the inputs array");
+    const int64_t bytes = numel * eb;
+    int nout = 0;
+    for (int r = 0; r < W; ++r) {
+        if (!rank_bufs[r]) return fail(RR_ERR_INVALID_ARG, "rank_bufs[%d] is NULL", r);
+        if (!aligned16(rank_bufs[r])) return fail(RR_ERR_ALIGNMENT, "rank_bufs[%d] not 16-byte aligned", r);
+        if (copy_mode && !inputs[r]) return fail(RR_ERR_INVALID_ARG, "inputs[%d] is NULL", r);
+        if (copy_mode && !aligned16(inputs[r])) return fail(RR_ERR_ALIGNMENT, "inputs[%d] not 16-byte aligned", r);
+        if (outputs[r]) {
+            if (!aligned16(outputs[r])) return fail(RR_ERR_ALIGNMENT, "outputs[%d] not 16-byte aligned", r);
+            ++nout;
+        }
+    }
+    if (nout == 0) return fail(RR_ERR_INVALID_ARG, "no output is materialised");
+    for (int i = 0; i < W; ++i) {
+        for (int j = 0; j < W; ++j) {
+            const Span bi = span_of(rank_bufs[i], bytes);
+            if (j > i && overlaps(bi, span_of(rank_bufs[j], bytes)))
+                return fail(RR_ERR_ALIAS, "rank_bufs[%d] and rank_bufs[%d] overlap", i, j);
+            if (copy_mode && overlaps(bi, span_of(inputs[j], bytes)))
+                return fail(RR_ERR_ALIAS, "rank_bufs[%d] and inputs[%d] overlap", i, j);
+            if (outputs[j] && overlaps(bi, span_of(outputs[j], bytes)))
+                return fail(RR_ERR_ALIAS, "rank_bufs[%d] and outputs[%d] overlap", i, j);
+            if (!outputs[i]) continue;
+            const Span oi = span_of(outputs[i], bytes);
+            if (j > i && outputs[j] && overlaps(oi, span_of(outputs[j], bytes)))
+                return fail(RR_ERR_ALIAS, "outputs[%d] and outputs[%d] overlap", i, j);
+            if (copy_mode && overlaps(oi, span_of(inputs[j], bytes)))
+                return fail(RR_ERR_ALIAS, "outputs[%d] and inputs[%d] overlap", i, j);
+        }
+    }
+    if (numel == 0) return ok();
+
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    uint32_t *scratch = nullptr;
+    uint32_t gen = 0;
+    {
+        // First call on this device: look up the array's device address with
+        // this device current (the host-side name is not a device address).
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        auto it = g_noalloc.find(dev);
+        if (it == g_noalloc.end()) {
+            void *addr = nullptr;
+            e = cudaGetSymbolAddress(&addr, noalloc_scratch);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(noalloc_scratch)");
+            it = g_noalloc.emplace(dev, NoAllocDevice{static_cast<uint32_t *>(addr), 0u}).first;
+        }
+        it->second.gen += 1;
+        if (it->second.gen == 0) it->second.gen = 2;
+        scratch = it->second.scratch;
+        gen = it->second.gen;
+    }
+
+    const rr::KernelChoice k = rr::oneshot_kernel_for(dtype, W);
+    int resident = 0;
+    rr_status st = resident_blocks(dev, k, &resident);
+    if (st != RR_OK) return st;
+    int cap = resident / W;
+    if (cap > kNoAllocMaxBlocks) cap = kNoAllocMaxBlocks;
+    if (cap < 1) return fail(RR_ERR_TOO_MANY_BLOCKS, "%d ranks do not fit on the device at once", W);
+    int64_t moved = (int64_t)nout * bytes * (W + 1) + (copy_mode ? 2 * (int64_t)W * bytes : 0);
+    int64_t want = (moved + (int64_t)W * kBytesPerBlock - 1) / ((int64_t)W * kBytesPerBlock);
+    const int B = (int)(want < 1 ? 1 : (want < cap ? want : cap));
+
+    // The array keeps the last call's words: the status words must start at
+    // zero (a timeout left by an earlier call would stop this one); the flags
+    // need no clearing, because a slot only matches this call's generation.
+    e = cudaMemsetAsync(scratch + kNoAllocFlagWords, 0, rr::kStatusWords * sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status words)");
+
+    rr::ReduceArgs a;
+    std::memset(&a, 0, sizeof a);
+    for (int r = 0; r < W; ++r) {
+        a.in[r] = copy_mode ? inputs[r] : nullptr;
+        a.buf[r] = rank_bufs[r];
+        a.out[r] = outputs[r];
+        if (outputs[r]) a.qlist[a.nout++] = r;
+    }
+    a.numel = numel;
+    a.nvec = bytes / 16;
+    a.W = W;
+    a.B = B;
+    a.copy_mode = copy_mode ? 1 : 0;
+    a.sig.flags = scratch;
+    a.sig.status = scratch + kNoAllocFlagWords;
+    a.sig.timeout_ns = rr::kDefaultTimeoutNs;
+    a.sig.max_spins = (uint32_t)(rr::kDefaultTimeoutNs / 64 + 4096);
+    a.sig.g = gen;
+    a.sig.W = W;
+    a.sig.Bmax = kNoAllocMaxBlocks;
+    a.sig.inject = -1;
+
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)(W * B), 1, 1);
+    cfg.blockDim = dim3((unsigned)k.threads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)k.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *params[1] = {&a};
+    e = cudaLaunchKernelExC(&cfg, k.fn, params);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC");
+    return ok();
+}

@@ -236,6 +236,36 @@ rr_status rr_allgather_param_contiguous(const void *const *rank_bufs, void *cons
                                         int num_splits, rr_dtype dtype, rr_signal_pad *pad,
                                         cudaStream_t stream);
 
+/*
+ * rr_allreduce_oneshot_noalloc -- rr_allreduce_oneshot for callers that may
+ * not allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * such as engine plugins whose enqueue runs inside a memory budget fixed
+ * ahead of time, frameworks that hand every byte of device memory to their
+ * own pool, and code on a latency-critical path where cudaMalloc's implicit
+ * device synchronisation would stall the GPU.  Those callers cannot create a
+ * signal pad (rr_signal_pad_create calls cudaMalloc).  This call uses instead
+ * a fixed signal pad that the library holds in a static device array of
+ * 64 KiB + 32 bytes, present on every GPU that loads the library until the
+ * process exits.  It calls no cudaMalloc, cudaFree or allocating routine.
+ *
+ * Arguments, results and errors are those of rr_allreduce_oneshot without
+ * the pad.  Limits: world_size 1..8 (larger W returns RR_ERR_INVALID_ARG
+ * with a message naming the limit) and at most 32 blocks per rank (chosen
+ * automatically).  The first call on a device looks up the array's device
+ * address with that device current; make that first call before any stream
+ * capture.  Every call on a device shares the one array: calls that overlap
+ * on the GPU (different streams, or other threads) race on it, so serialise
+ * them.  Each call clears the array's status words on `stream` before its
+ * kernel; a barrier timeout is not reported back (the kernel stops early and
+ * its outputs are incomplete), which happens only if the GPU cannot keep all
+ * ranks' blocks running at once for 2 s.
+ */
+rr_status rr_allreduce_oneshot_noalloc(const void *const *inputs, void *const *rank_bufs,
+                                       void *const *outputs, int world_size, int64_t numel,
+                                       rr_dtype dtype, int copy_mode, cudaStream_t stream);
+
 /* Name of a status code (static string). */
 const char *rr_status_string(rr_status s);
 
