@@ -127,6 +127,22 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def max_over_ranks(x, world):
+    """Max of a float over all ranks of the default process group (NCCL or
+    gloo); x itself when there is one rank."""
+    if world <= 1:
+        return float(x)
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
 # ---------------------------------------------------------------------- GPU arm
 
 class Step:
@@ -338,35 +354,28 @@ def run_gpu(args, rank, world, local_rank):
               for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(world)
     torch.cuda.synchronize()
     t_start.record(stream)
     for k in range(args.steps):
         step.run(events[k])
     t_end.record(stream)
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(world)
     clocks = sampler.stop() if rank == 0 else None
     step.pad.status(stream)
     elapsed_ms = t_start.elapsed_time(t_end)
     per_op_ms = {name: [events[k][i][0].elapsed_time(events[k][i][1]) for k in range(args.steps)]
                  for i, name in enumerate(ops)}
 
-    max_ms = elapsed_ms
-    if world > 1:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        max_ms = float(t.item())
+    max_ms = max_over_ranks(elapsed_ms, world)
 
     # end to end through the public API: host inputs in, host outputs out
     e2e_steps = max(1, min(args.steps, 5))
     with torch.cuda.stream(stream):
         step.run_e2e()
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
@@ -375,11 +384,7 @@ def run_gpu(args, rank, world, local_rank):
             step.run_e2e()
         e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
     bi, bo = step.e2e_bytes()
 
     if rank != 0:
