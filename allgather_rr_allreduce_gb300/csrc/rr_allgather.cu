@@ -124,55 +124,6 @@ __global__ void __launch_bounds__(kLdstThreads) gather_kernel_ldst(const __grid_
 }
 
 // ------------------------------------------------------------------ tma engine
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void fence_mbar_init()
-{
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(sdst)),
-        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-__device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
-                 "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
-
 // The part of piece s the bulk engine takes: both ends 16-byte aligned.
 __device__ __forceinline__ bool bulk_part(const GatherArgs &a, int r, int s, int64_t x0, int64_t x1,
                                           int64_t &p0, int64_t &pend, int64_t &d0)
@@ -184,17 +135,6 @@ __device__ __forceinline__ bool bulk_part(const GatherArgs &a, int r, int s, int
     return pend > p0;
 }
 
-// Bounded wait for the load of a stage; false after the pad's timeout.
-__device__ __forceinline__ bool stage_wait(const GatherArgs &a, uint64_t *bar, uint32_t parity)
-{
-    const uint64_t t0 = global_ns();
-    for (uint32_t spins = 0; !mbar_try_wait(bar, parity); ++spins) {
-        if ((spins & 255u) == 255u &&
-            ((global_ns() - t0) > a.sig.timeout_ns || spins > a.sig.max_spins))
-            return false;
-    }
-    return true;
-}
 
 __global__ void __launch_bounds__(kTmaThreads) gather_kernel_tma(const __grid_constant__ GatherArgs a)
 {
@@ -268,12 +208,12 @@ __global__ void __launch_bounds__(kTmaThreads) gather_kernel_tma(const __grid_co
         bool ok = true;
         for (int k = 0; k < nissued; ++k) {
             const int st = k % kTmaStages;
-            if (!stage_wait(a, &full[st], (uint32_t)(k / kTmaStages) & 1u)) {
+            if (!mbar_wait_bounded(a.sig, &full[st], (uint32_t)(k / kTmaStages) & 1u)) {
                 ok = false;
                 // Let the loads already in flight land before this block's
                 // shared memory can be handed to anyone else.
-                for (int j = k + 1; j < nissued; ++j)
-                    (void)stage_wait(a, &full[j % kTmaStages], (uint32_t)(j / kTmaStages) & 1u);
+                for (int j = k; j < nissued; ++j)
+                    (void)mbar_wait_bounded(a.sig, &full[j % kTmaStages], (uint32_t)(j / kTmaStages) & 1u);
                 break;
             }
             fence_async_shared();

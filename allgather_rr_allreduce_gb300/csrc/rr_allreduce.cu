@@ -19,26 +19,30 @@ namespace rr {
 
 constexpr int kReduceThreads = 256;
 
-// Vectors kept in flight per thread: 16 loads of 16 bytes whatever W is.
-template <int WMAX>
+// Vectors kept in flight per thread: 16 loads of 16 bytes whatever W is when
+// the reduction reads HBM; half as many when it reads bytes staged one round
+// earlier (still in L2, shorter latency, and the staging copy needs the
+// registers).
+template <int WMAX, bool kFromL2>
 struct Unroll {
-    static constexpr int U = WMAX >= 16 ? 1 : 16 / WMAX;
+    static constexpr int kLoads = kFromL2 ? 8 : 16;
+    static constexpr int U = WMAX >= kLoads ? 1 : kLoads / WMAX;
 };
 
 // dst[v] = combine over r of buf[r][v], for v in [v0, v1).  Thread t takes
 // vectors v0 + t, v0 + t + 256, ...: each warp load is 512 contiguous bytes.
-template <class Op, int WMAX>
+template <class Op, int WMAX, bool kFromL2, int kThreads = kReduceThreads>
 __device__ __forceinline__ void reduce_vectors(const ReduceArgs &a, void *dst_base, int64_t v0,
                                                int64_t v1)
 {
-    constexpr int U = Unroll<WMAX>::U;
+    constexpr int U = Unroll<WMAX, kFromL2>::U;
     uint4 *dst = static_cast<uint4 *>(dst_base);
     const int W = a.W;
-    for (int64_t base = v0 + threadIdx.x; base < v1; base += (int64_t)kReduceThreads * U) {
+    for (int64_t base = v0 + threadIdx.x; base < v1; base += (int64_t)kThreads * U) {
         uint4 x[U][WMAX];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int64_t v = base + (int64_t)u * kReduceThreads;
+            const int64_t v = base + (int64_t)u * kThreads;
             if (v < v1) {
 #pragma unroll
                 for (int r = 0; r < WMAX; ++r)
@@ -47,8 +51,40 @@ __device__ __forceinline__ void reduce_vectors(const ReduceArgs &a, void *dst_ba
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int64_t v = base + (int64_t)u * kReduceThreads;
+            const int64_t v = base + (int64_t)u * kThreads;
             if (v < v1) st_vec(dst + v, combine<Op, WMAX>(x[u], W));
+        }
+    }
+}
+
+// Reduce vectors [v0, v1) of the W rank buffers once and store the sum into
+// every output (the two-shot's allgather done as a broadcast by the owner of
+// the chunk, as the owner-side multicast store of the Triton kernel does).
+template <class Op, int WMAX, bool kFromL2, int kThreads = kReduceThreads>
+__device__ __forceinline__ void reduce_vectors_bcast(const ReduceArgs &a, int64_t v0, int64_t v1)
+{
+    constexpr int U = Unroll<WMAX, kFromL2>::U;
+    const int W = a.W;
+    for (int64_t base = v0 + threadIdx.x; base < v1; base += (int64_t)kThreads * U) {
+        uint4 x[U][WMAX];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = base + (int64_t)u * kThreads;
+            if (v < v1) {
+#pragma unroll
+                for (int r = 0; r < WMAX; ++r)
+                    if (r < W) x[u][r] = ld_vec(static_cast<const uint4 *>(a.buf[r]) + v);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = base + (int64_t)u * kThreads;
+            if (v < v1) {
+                const uint4 y = combine<Op, WMAX>(x[u], W);
+#pragma unroll
+                for (int q = 0; q < WMAX; ++q)
+                    if (q < W) st_vec(static_cast<uint4 *>(a.out[q]) + v, y);
+            }
         }
     }
 }
@@ -74,11 +110,42 @@ __device__ __forceinline__ void copy_vectors(const void *src_base, void *dst_bas
     }
 }
 
+// Several copies at once: dst_j[v] = src_j[v] for v < n_j, j < ncopies.
+// The copies' descriptors sit in shared memory (written by the caller before
+// a CTA barrier).  Thread t moves vector t (+ 256 i) of up to 8 copies per
+// pass, so the copies' loads are in flight together instead of one copy's
+// round trip after another.
+struct CopyDesc {
+    const uint4 *src;
+    uint4 *dst;
+    int64_t n;
+};
+
+__device__ __forceinline__ void copy_vectors_multi(const CopyDesc *d, int ncopies, int64_t longest)
+{
+    constexpr int kBatch = 8;
+    for (int64_t v = threadIdx.x; v < longest; v += kReduceThreads) {
+        for (int j0 = 0; j0 < ncopies; j0 += kBatch) {
+            uint4 x[kBatch];
+#pragma unroll
+            for (int jj = 0; jj < kBatch; ++jj) {
+                const int j = j0 + jj;
+                if (j < ncopies && v < d[j].n) x[jj] = ld_vec(d[j].src + v);
+            }
+#pragma unroll
+            for (int jj = 0; jj < kBatch; ++jj) {
+                const int j = j0 + jj;
+                if (j < ncopies && v < d[j].n) st_vec(d[j].dst + v, x[jj]);
+            }
+        }
+    }
+}
+
 // Elements [e0, e0 + n) of the ragged tail, copied one element at a time.
 template <int kBytes>
 __device__ __forceinline__ void copy_tail(const void *src, void *dst, int64_t e0, int n)
 {
-    for (int i = threadIdx.x; i < n; i += kReduceThreads) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
         if constexpr (kBytes == 2)
             static_cast<unsigned short *>(dst)[e0 + i] = __ldcg(static_cast<const unsigned short *>(src) + e0 + i);
         else
@@ -86,20 +153,44 @@ __device__ __forceinline__ void copy_tail(const void *src, void *dst, int64_t e0
     }
 }
 
+// Block (r, b)'s share of reducing vectors [s0, s1) into the kept outputs:
+// the nout x (s1 - s0) (output, vector) pairs are split evenly over the W
+// blocks of index b.  With every output kept, block (r, b) reduces exactly
+// rank r's own output, as rank r's kernel would; with fewer, the blocks of
+// ranks whose output is not kept lend their bandwidth.  Every block of index
+// b has passed the same barrier on these vectors, so what each may read is
+// the same.
+template <class Op, int WMAX, bool kFromL2, int kThreads = kReduceThreads>
+__device__ __forceinline__ void reduce_share(const ReduceArgs &a, int r, int64_t s0, int64_t s1)
+{
+    const int64_t L = s1 - s0;
+    if (L <= 0) return;
+    const int64_t total = (int64_t)a.nout * L;
+    int64_t pos = split_point(total, a.W, r);
+    const int64_t hi = split_point(total, a.W, r + 1);
+    while (pos < hi) {
+        const int m = (int)(pos / L);
+        const int64_t end = min(hi, (int64_t)(m + 1) * L);
+        const int64_t off = pos - (int64_t)m * L;
+        reduce_vectors<Op, WMAX, kFromL2, kThreads>(a, a.out[a.qlist[m]], s0 + off, s0 + off + (end - pos));
+        pos = end;
+    }
+}
+
 // ------------------------------------------------------------------ one-shot
 // Block b of every rank works on chunk b (vectors part_range(nvec, B, b); the
 // ragged tail belongs to the last chunk).
-//  copy_mode: stage inputs[r] chunk b into rank_bufs[r], STAGE barrier on
-//             block b (block b of every rank has staged chunk b).
-//  otherwise: ARRIVE barrier (block 0 of every rank has started).
-//  Reduce chunk b for the materialised outputs.  With every output
-//  materialised, block (r, b) reduces chunk b of output r, as rank r's own
-//  kernel would.  With fewer, the W blocks of chunk b share that chunk's
-//  outputs evenly, so the bandwidth of ranks whose output is not kept is not
-//  left idle; every one of them has passed the same barrier on chunk b.
+//  copy_mode off: ARRIVE barrier (block 0 of every rank has started, so every
+//      registered buffer holds its rank's data), reduce chunk b, END.
+//  copy_mode on: the chunk is pipelined in rounds of round_vec vectors.
+//      Round k: block (r, b) stages round k of its chunk from inputs[r] into
+//      rank_bufs[r] and emits round flag k (STAGE); it waits for round flag
+//      k of block b of every rank and reduces round k.  Staging of round k+1
+//      is issued before the wait on round k, so the flag latency hides behind
+//      the copy, and the staged bytes are read back while still in L2.
 //  END barrier on block b: no rank leaves while a peer still reads its chunk.
-template <class Op, int WMAX>
-__global__ void __launch_bounds__(kReduceThreads)
+template <class Op, int WMAX, bool kCopy>
+__global__ void __launch_bounds__(kReduceThreads, 2)
     oneshot_kernel(const __grid_constant__ ReduceArgs a)
 {
     __shared__ int s_ok;
@@ -110,34 +201,41 @@ __global__ void __launch_bounds__(kReduceThreads)
     part_range(a.nvec, a.B, b, v0, v1);
     const int64_t t0 = a.nvec * Op::kEPV;
     const int ntail = (int)(a.numel - t0);
+    const bool has_tail = last && ntail > 0;
 
-    if (a.copy_mode) {
-        copy_vectors(static_cast<const uint4 *>(a.in[r]) + v0, static_cast<uint4 *>(a.buf[r]) + v0, v1 - v0);
-        if (last && ntail > 0) copy_tail<Op::kBytes>(a.in[r], a.buf[r], t0, ntail);
-        emit(a.sig, RR_BARRIER_STAGE, r, b);
-        if (!wait(a.sig, RR_BARRIER_STAGE, r, b, &s_ok)) return;
+    if constexpr (kCopy) {
+        const int64_t P = a.round_vec;
+        int R = (int)((v1 - v0 + P - 1) / P);
+        if (R == 0 && has_tail) R = 1;
+        for (int k = -1; k < R; ++k) {
+            // stage round k + 1, then reduce round k
+            const int ks = k + 1;
+            if (ks < R) {
+                const int64_t s0 = v0 + (int64_t)ks * P;
+                const int64_t s1 = min(v1, s0 + P);
+                if (s1 > s0)
+                    copy_vectors(static_cast<const uint4 *>(a.in[r]) + s0, static_cast<uint4 *>(a.buf[r]) + s0,
+                                 s1 - s0);
+                if (ks == R - 1 && has_tail) copy_tail<Op::kBytes>(a.in[r], a.buf[r], t0, ntail);
+                emit_round(a.sig, 0, r, b, ks);
+            }
+            if (k < 0) continue;
+            if (!wait_round(a.sig, 0, r, b, k, &s_ok)) return;
+            const int64_t s0 = v0 + (int64_t)k * P;
+            reduce_share<Op, WMAX, true>(a, r, s0, min(v1, s0 + P));
+            if (k == R - 1 && has_tail)
+                for (int m = r; m < a.nout; m += a.W)
+                    for (int e = threadIdx.x; e < ntail; e += kReduceThreads)
+                        combine_scalar<Op>(a.buf, a.W, a.out[a.qlist[m]], t0 + e);
+        }
     } else {
         if (b == 0) emit(a.sig, RR_BARRIER_ARRIVE, r, 0);
         if (!wait(a.sig, RR_BARRIER_ARRIVE, r, 0, &s_ok)) return;
-    }
-
-    const int64_t L = v1 - v0;
-    if (L > 0) {
-        const int64_t total = (int64_t)a.nout * L;
-        int64_t pos = split_point(total, a.W, r);
-        const int64_t hi = split_point(total, a.W, r + 1);
-        while (pos < hi) {
-            const int m = (int)(pos / L);
-            const int64_t end = min(hi, (int64_t)(m + 1) * L);
-            const int64_t off = pos - (int64_t)m * L;
-            reduce_vectors<Op, WMAX>(a, a.out[a.qlist[m]], v0 + off, v0 + off + (end - pos));
-            pos = end;
-        }
-    }
-    if (last && ntail > 0) {
-        for (int m = r; m < a.nout; m += a.W)
-            for (int e = threadIdx.x; e < ntail; e += kReduceThreads)
-                combine_scalar<Op>(a.buf, a.W, a.out[a.qlist[m]], t0 + e);
+        reduce_share<Op, WMAX, false>(a, r, v0, v1);
+        if (has_tail)
+            for (int m = r; m < a.nout; m += a.W)
+                for (int e = threadIdx.x; e < ntail; e += kReduceThreads)
+                    combine_scalar<Op>(a.buf, a.W, a.out[a.qlist[m]], t0 + e);
     }
 
     emit(a.sig, RR_BARRIER_END, r, b);
@@ -146,85 +244,583 @@ __global__ void __launch_bounds__(kReduceThreads)
 
 // ------------------------------------------------------------------ two-shot
 // Rank c owns segment owned_segment(nvec, W, c); block b handles chunk b of
-// every segment (owned_chunk).  The ragged tail is owned by rank W-1.
-//  copy_mode: block b of rank r stages, from inputs[r], chunk b of every
-//             owner's segment (everything block b of any rank will read),
-//             then the STAGE barrier on block b; otherwise ARRIVE.
-//  Reduce-scatter: block (r, b) reduces chunk b of rank r's own segment into
-//             outputs[r].  MID barrier on block b.
-//  Allgather: block (r, b) copies chunk b of every other owner c's reduced
-//             segment from outputs[c] into outputs[r], starting at c = r + 1
-//             so that the ranks spread over different sources.  END barrier.
-template <class Op, int WMAX>
-__global__ void __launch_bounds__(kReduceThreads)
+// every segment (owned_chunk), pipelined in rounds of round_vec vectors (the
+// same number of rounds for block b of every rank: that of the longest chunk
+// b).  The ragged tail is owned by rank W-1 and handled in the last round of
+// the last block.
+//  copy_mode: round k of block (r, b) first stages, from inputs[r], round k
+//      of chunk b of every owner's segment (all that block b of any rank will
+//      read in round k) and emits round flag k (STAGE); otherwise one ARRIVE
+//      barrier at the start.
+//  Reduce-scatter, round k: wait for STAGE round k (copy_mode), reduce round
+//      k of rank r's own chunk into outputs[r], emit round flag k (MID).
+//  Allgather, round k: wait for MID round k of block b of every rank, copy
+//      round k of every other owner c's chunk from outputs[c] into
+//      outputs[r], all W-1 copies in flight together.
+//  Each wait comes one round after its emit (the next round's staging or
+//  reduction is issued in between), so the flag latency is hidden and the
+//  reduced chunk is copied out while it is still in L2.  END barrier.
+template <class Op, int WMAX, bool kCopy, bool kPush>
+__global__ void __launch_bounds__(kReduceThreads, 2)
     twoshot_kernel(const __grid_constant__ ReduceArgs a)
 {
     __shared__ int s_ok;
+    __shared__ CopyDesc s_desc[RR_MAX_WORLD];
+    __shared__ int64_t s_longest;
+    __shared__ int64_t s_c0[RR_MAX_WORLD], s_c1[RR_MAX_WORLD];  // chunk b of every owner
+    __shared__ int s_R;
     const int W = a.W;
     const int r = blockIdx.x / a.B;
     const int b = blockIdx.x - r * a.B;
     const bool last = b == a.B - 1;
     const int64_t t0 = a.nvec * Op::kEPV;
     const int ntail = (int)(a.numel - t0);
-    int64_t c0, c1;
+    const bool has_tail = last && ntail > 0;
+    const int64_t P = a.round_vec;
 
-    if (a.copy_mode) {
-        for (int c = 0; c < W; ++c) {
-            owned_chunk(a.nvec, W, a.B, c, b, c0, c1);
-            copy_vectors(static_cast<const uint4 *>(a.in[r]) + c0, static_cast<uint4 *>(a.buf[r]) + c0, c1 - c0);
+    if ((int)threadIdx.x < W) {
+        int64_t c0, c1;
+        owned_chunk(a.nvec, W, a.B, threadIdx.x, b, c0, c1);
+        s_c0[threadIdx.x] = c0;
+        s_c1[threadIdx.x] = c1;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int64_t longest = 0;
+        for (int c = 0; c < W; ++c) longest = max(longest, s_c1[c] - s_c0[c]);
+        int R = (int)((longest + P - 1) / P);
+        if (R == 0 && has_tail) R = 1;
+        s_R = R;
+    }
+    __syncthreads();
+    const int R = s_R;
+
+    // vectors [s0, s1) of round k of chunk b of owner c
+    auto round_of = [&](int c, int k, int64_t &s0, int64_t &s1) {
+        const int64_t c1 = s_c1[c];
+        s0 = min(c1, s_c0[c] + (int64_t)k * P);
+        s1 = min(c1, s0 + P);
+    };
+    // Copies of round k: staging (inputs[r] -> rank_bufs[r], every owner's
+    // chunk) or gathering (outputs[c] -> outputs[r], every other owner c).
+    auto copy_round = [&](int k, bool staging) {
+        const int ncopies = staging ? W : W - 1;
+        __syncthreads();
+        if ((int)threadIdx.x < ncopies) {
+            const int c = staging ? (int)threadIdx.x : (r + 1 + (int)threadIdx.x) % W;
+            int64_t s0, s1;
+            round_of(c, k, s0, s1);
+            const void *src = staging ? a.in[r] : a.out[c];
+            void *dst = staging ? a.buf[r] : a.out[r];
+            s_desc[threadIdx.x] = CopyDesc{static_cast<const uint4 *>(src) + s0, static_cast<uint4 *>(dst) + s0,
+                                           s1 - s0};
         }
-        if (last && ntail > 0) copy_tail<Op::kBytes>(a.in[r], a.buf[r], t0, ntail);
-        emit(a.sig, RR_BARRIER_STAGE, r, b);
-        if (!wait(a.sig, RR_BARRIER_STAGE, r, b, &s_ok)) return;
+        if (threadIdx.x == 0) {
+            int64_t m = 0;
+            for (int j = 0; j < ncopies; ++j) {
+                int64_t s0, s1;
+                round_of(staging ? j : (r + 1 + j) % W, k, s0, s1);
+                m = max(m, s1 - s0);
+            }
+            s_longest = m;
+        }
+        __syncthreads();
+        copy_vectors_multi(s_desc, ncopies, s_longest);
+        if (k == R - 1 && has_tail) {
+            if (staging) copy_tail<Op::kBytes>(a.in[r], a.buf[r], t0, ntail);
+            else if (r != W - 1) copy_tail<Op::kBytes>(a.out[W - 1], a.out[r], t0, ntail);
+        }
+    };
+    auto reduce_own = [&](int k) {
+        int64_t s0, s1;
+        round_of(r, k, s0, s1);
+        reduce_vectors<Op, WMAX, kCopy>(a, a.out[r], s0, s1);
+        if (k == R - 1 && has_tail && r == W - 1)
+            for (int e = threadIdx.x; e < ntail; e += kReduceThreads)
+                combine_scalar<Op>(a.buf, W, a.out[r], t0 + e);
+    };
+
+    if constexpr (kPush) {
+        // Allgather by broadcast: the owner stores its reduced chunk into
+        // every rank's output, so no rank reads a reduced segment back and no
+        // middle barrier is needed; END orders the completion.
+        auto reduce_push = [&](int k) {
+            int64_t s0, s1;
+            round_of(r, k, s0, s1);
+            reduce_vectors_bcast<Op, WMAX, kCopy>(a, s0, s1);
+            if (k == R - 1 && has_tail && r == W - 1)
+                for (int e = threadIdx.x; e < ntail; e += kReduceThreads)
+                    for (int q = 0; q < W; ++q) combine_scalar<Op>(a.buf, W, a.out[q], t0 + e);
+        };
+        if constexpr (kCopy) {
+            // iteration k: stage k+1; reduce and broadcast k
+            for (int k = -1; k < R; ++k) {
+                if (k + 1 < R) {
+                    copy_round(k + 1, true);
+                    emit_round(a.sig, 0, r, b, k + 1);
+                }
+                if (k >= 0) {
+                    if (!wait_round(a.sig, 0, r, b, k, &s_ok)) return;
+                    reduce_push(k);
+                }
+            }
+        } else {
+            if (b == 0) emit(a.sig, RR_BARRIER_ARRIVE, r, 0);
+            if (!wait(a.sig, RR_BARRIER_ARRIVE, r, 0, &s_ok)) return;
+            for (int k = 0; k < R; ++k) reduce_push(k);
+        }
+    } else if constexpr (kCopy) {
+        // iteration k: stage k+1; reduce k; gather k-1
+        for (int k = -1; k <= R; ++k) {
+            if (k + 1 < R) {
+                copy_round(k + 1, true);
+                emit_round(a.sig, 0, r, b, k + 1);
+            }
+            if (k >= 0 && k < R) {
+                if (!wait_round(a.sig, 0, r, b, k, &s_ok)) return;
+                reduce_own(k);
+                emit_round(a.sig, 1, r, b, k);
+            }
+            if (k >= 1) {
+                if (!wait_round(a.sig, 1, r, b, k - 1, &s_ok)) return;
+                copy_round(k - 1, false);
+            }
+        }
     } else {
         if (b == 0) emit(a.sig, RR_BARRIER_ARRIVE, r, 0);
         if (!wait(a.sig, RR_BARRIER_ARRIVE, r, 0, &s_ok)) return;
+        // iteration k: reduce k+1; gather k
+        for (int k = -1; k < R; ++k) {
+            if (k + 1 < R) {
+                reduce_own(k + 1);
+                emit_round(a.sig, 1, r, b, k + 1);
+            }
+            if (k >= 0) {
+                if (!wait_round(a.sig, 1, r, b, k, &s_ok)) return;
+                copy_round(k, false);
+            }
+        }
     }
-
-    owned_chunk(a.nvec, W, a.B, r, b, c0, c1);
-    reduce_vectors<Op, WMAX>(a, a.out[r], c0, c1);
-    if (last && ntail > 0 && r == W - 1)
-        for (int e = threadIdx.x; e < ntail; e += kReduceThreads)
-            combine_scalar<Op>(a.buf, W, a.out[r], t0 + e);
-
-    emit(a.sig, RR_BARRIER_MID, r, b);
-    if (!wait(a.sig, RR_BARRIER_MID, r, b, &s_ok)) return;
-
-    for (int k = 1; k < W; ++k) {
-        const int c = (r + k) % W;
-        owned_chunk(a.nvec, W, a.B, c, b, c0, c1);
-        copy_vectors(static_cast<const uint4 *>(a.out[c]) + c0, static_cast<uint4 *>(a.out[r]) + c0, c1 - c0);
-    }
-    if (last && ntail > 0 && r != W - 1) copy_tail<Op::kBytes>(a.out[W - 1], a.out[r], t0, ntail);
 
     emit(a.sig, RR_BARRIER_END, r, b);
     wait(a.sig, RR_BARRIER_END, r, b, &s_ok);
 }
 
+// ------------------------------------------------------------ one-shot, TMA
+// The one-shot with copy_mode off, its loads driven by the bulk-copy engine:
+// lane 0 of the last warp streams tiles of every rank's buffer into a ring of
+// shared-memory stages (cp.async.bulk, completion on a `full` mbarrier per
+// stage); eight consumer warps combine a tile's W vectors per thread and store
+// the sum, then release the stage on its `empty` mbarrier.  The loads stay in
+// flight while the consumers compute, so the HBM queue never drains between
+// iterations.  Work split, barriers and arithmetic are those of
+// oneshot_kernel.
+constexpr int kRtConsumerWarps = 8;
+constexpr int kRtThreads = 32 * (kRtConsumerWarps + 1);
+constexpr int kRtTileVec = 256;                 // vectors per rank per tile
+constexpr int kRtTileBytes = kRtTileVec * 16;   // 4 KiB
+template <int WMAX>
+struct RtStages {
+    static constexpr int kStages = (192 * 1024) / (WMAX * kRtTileBytes);  // 192 KiB of stages
+    static constexpr int kSmem = kStages * WMAX * kRtTileBytes;
+};
+
+// The block's share of chunk b cut into tiles that never cross an output:
+// tile i covers vectors [v, v + n) of output qlist[m].
+struct TileWalk {
+    int64_t pos, hi, L, v0;
+    __device__ bool next(int &m, int64_t &v, int &n)
+    {
+        if (pos >= hi) return false;
+        m = (int)(pos / L);
+        const int64_t end = min(hi, (int64_t)(m + 1) * L);
+        const int64_t len = min(end - pos, (int64_t)kRtTileVec);
+        v = v0 + (pos - (int64_t)m * L);
+        n = (int)len;
+        pos += len;
+        return true;
+    }
+};
+
+template <class Op, int WMAX>
+__global__ void __launch_bounds__(kRtThreads, 1)
+    oneshot_tma_kernel(const __grid_constant__ ReduceArgs a)
+{
+    constexpr int S = RtStages<WMAX>::kStages;
+    extern __shared__ __align__(128) unsigned char stages[];  // [S][WMAX][kRtTileBytes]
+    __shared__ __align__(8) uint64_t full[S];
+    __shared__ __align__(8) uint64_t empty[S];
+    __shared__ int s_ok;
+    __shared__ int s_fail;
+    const int W = a.W;
+    const int r = blockIdx.x / a.B;
+    const int b = blockIdx.x - r * a.B;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int64_t v0, v1;
+    part_range(a.nvec, a.B, b, v0, v1);
+    const int64_t t0 = a.nvec * Op::kEPV;
+    const int ntail = (int)(a.numel - t0);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kRtConsumerWarps);
+        }
+        fence_mbar_init();
+        s_fail = 0;
+    }
+    if (b == 0) emit(a.sig, RR_BARRIER_ARRIVE, r, 0);
+    else __syncthreads();
+    if (!wait(a.sig, RR_BARRIER_ARRIVE, r, 0, &s_ok)) return;
+
+    const int64_t L = v1 - v0;
+    TileWalk walk{0, 0, L > 0 ? L : 1, v0};
+    if (L > 0) {
+        const int64_t total = (int64_t)a.nout * L;
+        walk.pos = split_point(total, W, r);
+        walk.hi = split_point(total, W, r + 1);
+    }
+
+    if (warp == kRtConsumerWarps) {
+        if (lane == 0) {
+            int m, n;
+            int64_t v;
+            int i = 0;
+            bool ok = true;
+            while (walk.next(m, v, n)) {
+                const int st = i % S;
+                if (i >= S && !mbar_wait_bounded(a.sig, &empty[st], (uint32_t)((i / S) - 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                mbar_expect_tx(&full[st], (uint32_t)(W * n * 16));
+                for (int c = 0; c < W; ++c)
+                    bulk_load(stages + ((size_t)st * WMAX + c) * kRtTileBytes,
+                              static_cast<const uint4 *>(a.buf[c]) + v, (uint32_t)(n * 16), &full[st]);
+                ++i;
+            }
+            if (!ok) {
+                // Let every load already issued land before the block can exit.
+                for (int j = max(0, i - S); j < i; ++j)
+                    (void)mbar_wait_bounded(a.sig, &full[j % S], (uint32_t)(j / S) & 1u);
+                s_fail = 1;
+            }
+        }
+    } else {
+        int m, n;
+        int64_t v;
+        int i = 0;
+        while (walk.next(m, v, n)) {
+            const int st = i % S;
+            if (!mbar_wait_bounded(a.sig, &full[st], (uint32_t)(i / S) & 1u)) {
+                s_fail = 1;
+                break;
+            }
+            const int t = threadIdx.x;
+            if (t < n) {
+                uint4 x[WMAX];
+#pragma unroll
+                for (int c = 0; c < WMAX; ++c)
+                    if (c < W)
+                        x[c] = *reinterpret_cast<const uint4 *>(stages + ((size_t)st * WMAX + c) * kRtTileBytes +
+                                                                (size_t)t * 16);
+                st_vec(static_cast<uint4 *>(a.out[a.qlist[m]]) + v + t, combine<Op, WMAX>(x, W));
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+            ++i;
+        }
+        if (b == a.B - 1 && ntail > 0)
+            for (int mm = r; mm < a.nout; mm += W)
+                for (int e = threadIdx.x; e < ntail; e += 32 * kRtConsumerWarps)
+                    combine_scalar<Op>(a.buf, W, a.out[a.qlist[mm]], t0 + e);
+    }
+    __syncthreads();
+    if (s_fail) {
+        if (threadIdx.x == 0) record_timeout(a.sig, RR_BARRIER_END, r, b);
+        return;
+    }
+    emit(a.sig, RR_BARRIER_END, r, b);
+    wait(a.sig, RR_BARRIER_END, r, b, &s_ok);
+}
+
+// ------------------------------------------------- copy_mode, warp-specialised
+// copy_mode with the staging done by a producer warp through the bulk-copy
+// engine, for the one-shot and for the two-shot with a broadcast allgather.
+//
+// Producer (lane 0 of the last warp): copies, round by round, everything
+// block b of any rank will read from rank r into rank_bufs[r] (one-shot:
+// round k of chunk b; two-shot: round k of chunk b of every owner's segment)
+// as 16 KiB tiles through a ring of shared-memory stages: cp.async.bulk
+// global -> shared completing on a `full` mbarrier, then cp.async.bulk shared
+// -> global in a bulk group.  Loads run kSwAhead tiles ahead of the stores.
+// After each store it waits until at most kSwAhead - 1 bulk groups are
+// incomplete; every round whose tiles have all landed is then published:
+// async-proxy fence, round flag k (STAGE) released to every listener.  Only
+// this lane waits for the stores to land.
+// Consumers (the other 8 warps): per round, wait for round flag k of block b
+// of every rank (named barrier among themselves), then reduce round k from
+// the staged buffers, which the producers wrote moments ago (L2).
+// The ragged tail is staged by the consumers before the roles split, so the
+// producer's first release covers it.  END barrier over the whole block.
+constexpr int kSwConsumerWarps = 8;
+constexpr int kSwConsumers = 32 * kSwConsumerWarps;
+constexpr int kSwThreads = kSwConsumers + 32;
+constexpr int kSwStages = 8;
+constexpr int kSwAhead = 4;          // loads in flight ahead of the store being issued
+constexpr int kSwTileBytes = 16384;
+constexpr int kSwSmem = kSwStages * kSwTileBytes;
+static_assert(kSwAhead < kSwStages, "the ring must hold the loads ahead and the stores in flight");
+
+template <class Op, int WMAX, bool kTwoShot>
+__global__ void __launch_bounds__(kSwThreads, 1) staged_kernel(const __grid_constant__ ReduceArgs a)
+{
+    extern __shared__ __align__(128) unsigned char stages[];
+    __shared__ __align__(8) uint64_t full[kSwStages];
+    __shared__ int tile_round[kSwStages];
+    __shared__ int64_t tile_off[kSwStages];   // byte offset within the rank buffer
+    __shared__ uint32_t tile_len[kSwStages];
+    __shared__ int64_t s_c0[RR_MAX_WORLD], s_c1[RR_MAX_WORLD];
+    __shared__ int s_ok, s_fail, s_R;
+    const int W = a.W;
+    const int r = blockIdx.x / a.B;
+    const int b = blockIdx.x - r * a.B;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool last = b == a.B - 1;
+    const int64_t t0 = a.nvec * Op::kEPV;
+    const int ntail = (int)(a.numel - t0);
+    const bool has_tail = last && ntail > 0;
+    const int64_t P = a.round_vec;
+    const int nranges = kTwoShot ? W : 1;
+
+    // Chunk b: one-shot, the block's share of the message; two-shot, chunk
+    // b of every owner's segment (s_c0/s_c1 indexed by owner).
+    if ((int)threadIdx.x < nranges) {
+        int64_t c0, c1;
+        if (kTwoShot) owned_chunk(a.nvec, W, a.B, threadIdx.x, b, c0, c1);
+        else part_range(a.nvec, a.B, b, c0, c1);
+        s_c0[threadIdx.x] = c0;
+        s_c1[threadIdx.x] = c1;
+    }
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kSwStages; ++i) mbar_init(&full[i], 1);
+        fence_mbar_init();
+        s_fail = 0;
+    }
+    if (has_tail) copy_tail<Op::kBytes>(a.in[r], a.buf[r], t0, ntail);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int64_t longest = 0;
+        for (int j = 0; j < nranges; ++j) longest = max(longest, s_c1[j] - s_c0[j]);
+        int R = (int)((longest + P - 1) / P);
+        if (R == 0 && has_tail) R = 1;
+        s_R = R;
+    }
+    __syncthreads();
+    const int R = s_R;
+
+    if (warp == kSwConsumerWarps) {
+        if (lane == 0) {
+            // tile walk: round k, range j, byte position inside the range
+            int k = 0, j = 0;
+            int64_t pos = 0;
+            auto next_tile = [&](int &kr, int64_t &off, uint32_t &len) -> bool {
+                while (k < R) {
+                    if (j < nranges) {
+                        const int64_t c1 = s_c1[j];
+                        const int64_t rs = min(c1, s_c0[j] + (int64_t)k * P) * 16;
+                        const int64_t re = min(c1, s_c0[j] + (int64_t)(k + 1) * P) * 16;
+                        if (rs + pos < re) {
+                            off = rs + pos;
+                            const int64_t left = re - off;
+                            len = (uint32_t)(left < kSwTileBytes ? left : kSwTileBytes);
+                            pos += len;
+                            kr = k;
+                            return true;
+                        }
+                        ++j;
+                        pos = 0;
+                        continue;
+                    }
+                    ++k;
+                    j = 0;
+                    pos = 0;
+                }
+                return false;
+            };
+            const char *src = static_cast<const char *>(a.in[r]);
+            char *dst = static_cast<char *>(a.buf[r]);
+            int issued = 0;
+            auto issue = [&](int t) -> bool {
+                int kr;
+                int64_t off;
+                uint32_t len;
+                if (!next_tile(kr, off, len)) return false;
+                const int st = t % kSwStages;
+                tile_round[st] = kr;
+                tile_off[st] = off;
+                tile_len[st] = len;
+                mbar_expect_tx(&full[st], len);
+                bulk_load(stages + (size_t)st * kSwTileBytes, src + off, len, &full[st]);
+                return true;
+            };
+            while (issued < kSwAhead && issue(issued)) ++issued;
+            int published = 0;  // rounds whose flags are out
+            bool ok = true;
+            for (int t = 0; t < issued; ++t) {
+                const int st = t % kSwStages;
+                if (!mbar_wait_bounded(a.sig, &full[st], (uint32_t)(t / kSwStages) & 1u)) {
+                    ok = false;
+                    for (int u = t; u < issued; ++u)
+                        (void)mbar_wait_bounded(a.sig, &full[u % kSwStages], (uint32_t)(u / kSwStages) & 1u);
+                    break;
+                }
+                fence_async_shared();
+                bulk_store(dst + tile_off[st], stages + (size_t)st * kSwTileBytes, tile_len[st]);
+                bulk_commit();
+                // tiles <= t - (kSwAhead - 1) have landed (their stages are free too)
+                bulk_wait_pending<kSwAhead - 1>();
+                const int done = t - (kSwAhead - 1);
+                if (done >= 0) {
+                    // rounds before the round of tile done+1 are complete
+                    const int upto = (done + 1 < issued) ? tile_round[(done + 1) % kSwStages] : -1;
+                    if (upto > published) {
+                        fence_async_global();
+                        for (; published < upto; ++published) emit_round_single(a.sig, 0, r, b, published);
+                    }
+                }
+                if (issue(issued)) ++issued;
+            }
+            bulk_wait_all();
+            if (ok) {
+                fence_async_global();
+                for (; published < R; ++published) emit_round_single(a.sig, 0, r, b, published);
+            } else {
+                s_fail = 1;
+                record_timeout(a.sig, RR_BARRIER_STAGE, r, b);
+            }
+        }
+    } else {
+        const GroupSync sync{kSwConsumers};
+        for (int k = 0; k < R; ++k) {
+            if (!wait_round(a.sig, 0, r, b, k, &s_ok, sync)) {
+                if (threadIdx.x == 0) s_fail = 1;
+                break;
+            }
+            if constexpr (kTwoShot) {
+                const int64_t c1 = s_c1[r];
+                const int64_t rs = min(c1, s_c0[r] + (int64_t)k * P);
+                const int64_t re = min(c1, rs + P);
+                reduce_vectors_bcast<Op, WMAX, true, kSwConsumers>(a, rs, re);
+                if (k == R - 1 && has_tail && r == W - 1)
+                    for (int e = threadIdx.x; e < ntail; e += kSwConsumers)
+                        for (int q = 0; q < W; ++q) combine_scalar<Op>(a.buf, W, a.out[q], t0 + e);
+            } else {
+                const int64_t c1 = s_c1[0];
+                const int64_t rs = min(c1, s_c0[0] + (int64_t)k * P);
+                const int64_t re = min(c1, rs + P);
+                reduce_share<Op, WMAX, true, kSwConsumers>(a, r, rs, re);
+                if (k == R - 1 && has_tail)
+                    for (int m = r; m < a.nout; m += W)
+                        for (int e = threadIdx.x; e < ntail; e += kSwConsumers)
+                            combine_scalar<Op>(a.buf, W, a.out[a.qlist[m]], t0 + e);
+            }
+        }
+    }
+    __syncthreads();
+    if (s_fail) return;
+    emit(a.sig, RR_BARRIER_END, r, b);
+    wait(a.sig, RR_BARRIER_END, r, b, &s_ok);
+}
+
 // ------------------------------------------------------------------ dispatch
-template <class Op, bool kTwoShot>
-static KernelChoice pick(int W)
+template <class Op, bool kCopy>
+static const void *pick_oneshot(int W)
+{
+    if (W <= 2) return (const void *)oneshot_kernel<Op, 2, kCopy>;
+    if (W <= 4) return (const void *)oneshot_kernel<Op, 4, kCopy>;
+    if (W <= 8) return (const void *)oneshot_kernel<Op, 8, kCopy>;
+    return (const void *)oneshot_kernel<Op, 16, kCopy>;
+}
+
+template <class Op, bool kCopy, bool kPush>
+static const void *pick_twoshot(int W)
+{
+    if (W <= 2) return (const void *)twoshot_kernel<Op, 2, kCopy, kPush>;
+    if (W <= 4) return (const void *)twoshot_kernel<Op, 4, kCopy, kPush>;
+    if (W <= 8) return (const void *)twoshot_kernel<Op, 8, kCopy, kPush>;
+    return (const void *)twoshot_kernel<Op, 16, kCopy, kPush>;
+}
+
+template <class Op>
+static const void *pick_reduce(bool twoshot, int W, bool copy, bool push)
+{
+    if (!twoshot) return copy ? pick_oneshot<Op, true>(W) : pick_oneshot<Op, false>(W);
+    if (copy) return push ? pick_twoshot<Op, true, true>(W) : pick_twoshot<Op, true, false>(W);
+    return push ? pick_twoshot<Op, false, true>(W) : pick_twoshot<Op, false, false>(W);
+}
+
+static KernelChoice pick(rr_dtype dtype, bool twoshot, int W, bool copy, bool push)
 {
     const void *fn;
-    if (W <= 2) fn = kTwoShot ? (const void *)twoshot_kernel<Op, 2> : (const void *)oneshot_kernel<Op, 2>;
-    else if (W <= 4) fn = kTwoShot ? (const void *)twoshot_kernel<Op, 4> : (const void *)oneshot_kernel<Op, 4>;
-    else if (W <= 8) fn = kTwoShot ? (const void *)twoshot_kernel<Op, 8> : (const void *)oneshot_kernel<Op, 8>;
-    else fn = kTwoShot ? (const void *)twoshot_kernel<Op, 16> : (const void *)oneshot_kernel<Op, 16>;
+    switch (dtype) {
+    case RR_BF16: fn = pick_reduce<OpBF16>(twoshot, W, copy, push); break;
+    case RR_FP16: fn = pick_reduce<OpFP16>(twoshot, W, copy, push); break;
+    case RR_FP32: fn = pick_reduce<OpFP32>(twoshot, W, copy, push); break;
+    default: fn = pick_reduce<OpI32>(twoshot, W, copy, push); break;
+    }
     return KernelChoice{fn, kReduceThreads, 0};
 }
 
-template <bool kTwoShot>
-static KernelChoice pick_dtype(rr_dtype dtype, int W)
+KernelChoice oneshot_kernel_for(rr_dtype dtype, int W, bool copy_mode) { return pick(dtype, false, W, copy_mode, false); }
+
+template <class Op, bool kTwoShot>
+static const void *pick_staged_w(int W)
 {
-    switch (dtype) {
-    case RR_BF16: return pick<OpBF16, kTwoShot>(W);
-    case RR_FP16: return pick<OpFP16, kTwoShot>(W);
-    case RR_FP32: return pick<OpFP32, kTwoShot>(W);
-    default: return pick<OpI32, kTwoShot>(W);
-    }
+    if (W <= 2) return (const void *)staged_kernel<Op, 2, kTwoShot>;
+    if (W <= 4) return (const void *)staged_kernel<Op, 4, kTwoShot>;
+    if (W <= 8) return (const void *)staged_kernel<Op, 8, kTwoShot>;
+    return (const void *)staged_kernel<Op, 16, kTwoShot>;
 }
 
-KernelChoice oneshot_kernel_for(rr_dtype dtype, int W) { return pick_dtype<false>(dtype, W); }
-KernelChoice twoshot_kernel_for(rr_dtype dtype, int W) { return pick_dtype<true>(dtype, W); }
+KernelChoice staged_kernel_for(rr_dtype dtype, int W, bool twoshot)
+{
+    const void *fn;
+    switch (dtype) {
+    case RR_BF16: fn = twoshot ? pick_staged_w<OpBF16, true>(W) : pick_staged_w<OpBF16, false>(W); break;
+    case RR_FP16: fn = twoshot ? pick_staged_w<OpFP16, true>(W) : pick_staged_w<OpFP16, false>(W); break;
+    case RR_FP32: fn = twoshot ? pick_staged_w<OpFP32, true>(W) : pick_staged_w<OpFP32, false>(W); break;
+    default: fn = twoshot ? pick_staged_w<OpI32, true>(W) : pick_staged_w<OpI32, false>(W); break;
+    }
+    return KernelChoice{fn, kSwThreads, kSwSmem};
+}
+KernelChoice twoshot_kernel_for(rr_dtype dtype, int W, bool copy_mode, bool push)
+{
+    KernelChoice k = pick(dtype, true, W, copy_mode, push);
+    // The broadcast writes W output streams per block; without staging, one
+    // block per SM measured faster than two on GB300 (88 vs 94 us at W=8,
+    // 32 MiB per rank); with staging, two per SM are faster (176 vs 230 us).
+    if (push && !copy_mode) k.per_sm = 1;
+    return k;
+}
+
+template <class Op>
+static KernelChoice pick_tma(int W)
+{
+    if (W <= 2) return KernelChoice{(const void *)oneshot_tma_kernel<Op, 2>, kRtThreads, RtStages<2>::kSmem};
+    if (W <= 4) return KernelChoice{(const void *)oneshot_tma_kernel<Op, 4>, kRtThreads, RtStages<4>::kSmem};
+    if (W <= 8) return KernelChoice{(const void *)oneshot_tma_kernel<Op, 8>, kRtThreads, RtStages<8>::kSmem};
+    return KernelChoice{(const void *)oneshot_tma_kernel<Op, 16>, kRtThreads, RtStages<16>::kSmem};
+}
+
+KernelChoice oneshot_tma_kernel_for(rr_dtype dtype, int W)
+{
+    switch (dtype) {
+    case RR_BF16: return pick_tma<OpBF16>(W);
+    case RR_FP16: return pick_tma<OpFP16>(W);
+    case RR_FP32: return pick_tma<OpFP32>(W);
+    default: return pick_tma<OpI32>(W);
+    }
+}
 
 }  // namespace rr

@@ -20,11 +20,16 @@ struct rr_signal_pad {
     int Bmax;
     uint64_t timeout_ns;
     uint32_t *flags;   // device
+    uint64_t *rflags;  // device, round flags
     uint32_t *status;  // device, rr::kStatusWords words
-    uint32_t gen;      // generation of the last call (0 = none yet)
+    uint32_t gen;      // generation of the last call (0 = none yet): low 32 bits of gen64
+    uint64_t gen64;    // 64-bit call counter; round flags grow with it
+    int64_t round_bytes;  // 0 = automatic
     int inject;        // -1 or rank*4 + barrier
     int blocks_override;
-    int engine;        // 0 auto, 1 ldst, 2 tma
+    int engine;        // gathers: 0 auto, 1 ldst, 2 tma
+    int reduce_engine; // one-shot with copy_mode off: 0 auto, 1 ldst, 2 tma
+    int twoshot_mode;  // 0 auto, 1 pull (middle barrier), 2 push (owner broadcasts)
     int last_grid;
     int last_B;
     int last_engine;
@@ -109,6 +114,13 @@ rr_status resident_blocks(int dev, const rr::KernelChoice &k, int *out)
     return RR_OK;
 }
 
+int sm_count(int dev)
+{
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = g_sms.find(dev);
+    return it == g_sms.end() ? 0 : it->second;
+}
+
 // Blocks per rank: enough that each block moves about kBytesPerBlock, no
 // more than the pad allows, and few enough that all W*B blocks are resident
 // at once (the ranks' blocks wait on each other, so every one of them must
@@ -132,10 +144,26 @@ rr_status plan_blocks(rr_signal_pad *pad, const rr::KernelChoice &k, int W, int6
         *B = pad->blocks_override;
         return RR_OK;
     }
+    if (k.per_sm > 0) {
+        const int pref = k.per_sm * sm_count(pad->device) / W;
+        if (pref >= 1 && pref < cap) cap = pref;
+    }
     int64_t want = (total_bytes + (int64_t)W * kBytesPerBlock - 1) / ((int64_t)W * kBytesPerBlock);
     if (want < 1) want = 1;
     *B = (int)(want < cap ? want : cap);
     return RR_OK;
+}
+
+// Vectors per round of a pipelined chunk: `pref` by default (or the pad's
+// option), rounded to whole granules, and large enough that the longest
+// chunk needs fewer than 2^kRoundBits rounds.
+int64_t round_vectors(int64_t option_bytes, int64_t pref, int64_t longest_chunk)
+{
+    int64_t p = option_bytes > 0 ? option_bytes / 16 : pref;
+    const int64_t min_p = (longest_chunk + (1 << rr::kRoundBits) - 2) / ((1 << rr::kRoundBits) - 1);
+    if (p < min_p) p = min_p;
+    p = ((p + rr::kGranuleVec - 1) / rr::kGranuleVec) * rr::kGranuleVec;
+    return p < rr::kGranuleVec ? rr::kGranuleVec : p;
 }
 
 rr::SignalArgs signal_args(rr_signal_pad *pad)
@@ -146,9 +174,12 @@ rr::SignalArgs signal_args(rr_signal_pad *pad)
     s.timeout_ns = pad->timeout_ns;
     const uint64_t spins = pad->timeout_ns / 64 + 4096;
     s.max_spins = spins > 0xffffffffull ? 0xffffffffu : (uint32_t)spins;
-    pad->gen += 1;
-    if (pad->gen == 0) pad->gen = 2;  // never 0 (the pad starts zeroed); keep the parity
+    pad->gen64 += 1;
+    if ((uint32_t)pad->gen64 == 0) pad->gen64 += 2;  // g is never 0 (the pad starts zeroed); keep the parity
+    pad->gen = (uint32_t)pad->gen64;
     s.g = pad->gen;
+    s.rflags = pad->rflags;
+    s.rbase = pad->gen64 << rr::kRoundBits;
     s.W = pad->W;
     s.Bmax = pad->Bmax;
     s.inject = pad->inject;
@@ -246,7 +277,14 @@ rr_status allreduce_common(bool twoshot, const void *const *inputs, void *const 
     st = check_device(pad);
     if (st != RR_OK) return st;
 
-    const rr::KernelChoice k = twoshot ? rr::twoshot_kernel_for(dtype, W) : rr::oneshot_kernel_for(dtype, W);
+    const bool push = pad->twoshot_mode != 1;
+    // bulk-copy engine: one-shot loads (copy_mode off), or staging by a
+    // producer warp (copy_mode on; for the two-shot only with the push allgather)
+    const bool tma = pad->reduce_engine == 2 && (copy_mode ? (!twoshot || push) : !twoshot);
+    const rr::KernelChoice k = tma ? (copy_mode ? rr::staged_kernel_for(dtype, W, twoshot)
+                                                : rr::oneshot_tma_kernel_for(dtype, W))
+                               : twoshot ? rr::twoshot_kernel_for(dtype, W, copy_mode != 0, push)
+                                         : rr::oneshot_kernel_for(dtype, W, copy_mode != 0);
     int64_t moved = twoshot ? bytes * (W + 1) + (int64_t)(W - 1) * bytes * 2
                             : (int64_t)nout * bytes * (W + 1);
     if (copy_mode) moved += 2 * (int64_t)W * bytes;
@@ -267,9 +305,17 @@ rr_status allreduce_common(bool twoshot, const void *const *inputs, void *const 
     a.W = W;
     a.B = B;
     a.copy_mode = copy_mode ? 1 : 0;
+    {
+        // longest chunk of any block: one-shot chunks split the message, two-shot
+        // chunks split an owned segment
+        const int64_t ng = (a.nvec + rr::kGranuleVec - 1) / rr::kGranuleVec;
+        const int64_t seg = twoshot ? (ng + W - 1) / W : ng;
+        const int64_t longest = ((seg + B - 1) / B) * rr::kGranuleVec;
+        a.round_vec = round_vectors(pad->round_bytes, (tma && copy_mode) ? 8192 : twoshot ? 2048 : 4096, longest);
+    }
     a.sig = signal_args(pad);
     pad->last_B = B;
-    pad->last_engine = 1;
+    pad->last_engine = tma ? 2 : 1;
     return launch(pad, k, W * B, a, stream);
 }
 
@@ -358,7 +404,10 @@ rr_status rr_signal_pad_create(int world_size, int max_blocks_per_rank, uint64_t
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     const size_t nflags = (size_t)world_size * rr::kNumBarriers * 2 * (size_t)Bmax * (size_t)world_size;
-    const size_t bytes = (nflags + rr::kStatusWords) * sizeof(uint32_t);
+    const size_t nrflags = (size_t)world_size * rr::kRoundKinds * (size_t)Bmax * (size_t)world_size;
+    const size_t flag_bytes = ((nflags * sizeof(uint32_t) + 255) / 256) * 256;
+    const size_t rflag_bytes = nrflags * sizeof(uint64_t);
+    const size_t bytes = flag_bytes + rflag_bytes + rr::kStatusWords * sizeof(uint32_t);
     void *mem = nullptr;
     e = cudaMalloc(&mem, bytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(signal pad)");
@@ -375,7 +424,8 @@ rr_status rr_signal_pad_create(int world_size, int max_blocks_per_rank, uint64_t
     p->Bmax = Bmax;
     p->timeout_ns = timeout_ns ? timeout_ns : rr::kDefaultTimeoutNs;
     p->flags = static_cast<uint32_t *>(mem);
-    p->status = p->flags + nflags;
+    p->rflags = reinterpret_cast<uint64_t *>(static_cast<char *>(mem) + flag_bytes);
+    p->status = reinterpret_cast<uint32_t *>(static_cast<char *>(mem) + flag_bytes + rflag_bytes);
     p->inject = -1;
     *out = p;
     return ok();
@@ -452,6 +502,18 @@ rr_status rr_signal_pad_set_option(rr_signal_pad *pad, rr_option opt, int64_t va
             return fail(RR_ERR_INVALID_ARG, "inject %lld", (long long)value);
         pad->inject = (int)value;
         return ok();
+    case RR_OPT_ROUND_BYTES:
+        if (value < 0) return fail(RR_ERR_INVALID_ARG, "round_bytes %lld", (long long)value);
+        pad->round_bytes = value;
+        return ok();
+    case RR_OPT_REDUCE_ENGINE:
+        if (value < 0 || value > 2) return fail(RR_ERR_INVALID_ARG, "reduce engine %lld", (long long)value);
+        pad->reduce_engine = (int)value;
+        return ok();
+    case RR_OPT_TWOSHOT_MODE:
+        if (value < 0 || value > 2) return fail(RR_ERR_INVALID_ARG, "two-shot mode %lld", (long long)value);
+        pad->twoshot_mode = (int)value;
+        return ok();
     default: return fail(RR_ERR_INVALID_ARG, "option %d cannot be set", (int)opt);
     }
 }
@@ -464,6 +526,9 @@ rr_status rr_signal_pad_get_option(rr_signal_pad *pad, rr_option opt, int64_t *v
     case RR_OPT_BLOCKS_PER_RANK: *value = pad->blocks_override; break;
     case RR_OPT_GATHER_ENGINE: *value = pad->engine; break;
     case RR_OPT_INJECT_SKIP: *value = pad->inject; break;
+    case RR_OPT_ROUND_BYTES: *value = pad->round_bytes; break;
+    case RR_OPT_REDUCE_ENGINE: *value = pad->reduce_engine; break;
+    case RR_OPT_TWOSHOT_MODE: *value = pad->twoshot_mode; break;
     case RR_OPT_GENERATION: *value = pad->gen; break;
     case RR_OPT_LAST_GRID: *value = pad->last_grid; break;
     case RR_OPT_LAST_BLOCKS_PER_RANK: *value = pad->last_B; break;
@@ -537,20 +602,24 @@ constexpr int kNoAllocMaxWorld = 8;    // largest W the fixed pad can serve
 constexpr int kNoAllocMaxBlocks = 32;  // largest blocks per rank it can serve
 constexpr size_t kNoAllocFlagWords =
     (size_t)kNoAllocMaxWorld * kNoAllocMaxWorld * rr::kNumBarriers * 2 * kNoAllocMaxBlocks;
+constexpr size_t kNoAllocRoundWords =  // 32-bit words holding the 64-bit round flags
+    2 * (size_t)kNoAllocMaxWorld * kNoAllocMaxWorld * rr::kRoundKinds * kNoAllocMaxBlocks;
 
 struct NoAllocDevice {
     uint32_t *scratch;  // device address of noalloc_scratch on this device
-    uint32_t gen;       // generation of the last call on this device
+    uint64_t gen;       // generation of the last call on this device
 };
 std::mutex g_noalloc_mu;
 std::map<int, NoAllocDevice> g_noalloc;
 
 }  // namespace
 
-// Flags ([W][4 barriers][2 parities][32 blocks][W] for the call's W) followed
-// by the status words: 64 KiB + 32 B, zero at module load, on every device
-// that loads this library, held until the process exits.
-static __device__ __align__(256) uint32_t noalloc_scratch[kNoAllocFlagWords + rr::kStatusWords];
+// Flags ([W][4 barriers][2 parities][32 blocks][W] for the call's W), then the
+// 64-bit round flags ([W][2][32 blocks][W]), then the status words: 96 KiB +
+// 32 B, zero at module load, on every device that loads this library, held
+// until the process exits.
+static __device__ __align__(256) uint32_t
+    noalloc_scratch[kNoAllocFlagWords + kNoAllocRoundWords + rr::kStatusWords];
 
 extern "C" rr_status rr_allreduce_oneshot_noalloc(const void *const *inputs, void *const *rank_bufs,
                                                   void *const *outputs, int world_size, int64_t numel,
@@ -603,7 +672,7 @@ extern "C" rr_status rr_allreduce_oneshot_noalloc(const void *const *inputs, voi
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     uint32_t *scratch = nullptr;
-    uint32_t gen = 0;
+    uint64_t gen = 0;
     {
         // First call on this device: look up the array's device address with
         // this device current (the host-side name is not a device address).
@@ -616,12 +685,12 @@ extern "C" rr_status rr_allreduce_oneshot_noalloc(const void *const *inputs, voi
             it = g_noalloc.emplace(dev, NoAllocDevice{static_cast<uint32_t *>(addr), 0u}).first;
         }
         it->second.gen += 1;
-        if (it->second.gen == 0) it->second.gen = 2;
+        if ((uint32_t)it->second.gen == 0) it->second.gen += 2;
         scratch = it->second.scratch;
         gen = it->second.gen;
     }
 
-    const rr::KernelChoice k = rr::oneshot_kernel_for(dtype, W);
+    const rr::KernelChoice k = rr::oneshot_kernel_for(dtype, W, copy_mode != 0);
     int resident = 0;
     rr_status st = resident_blocks(dev, k, &resident);
     if (st != RR_OK) return st;
@@ -634,8 +703,9 @@ extern "C" rr_status rr_allreduce_oneshot_noalloc(const void *const *inputs, voi
 
     // The array keeps the last call's words: the status words must start at
     // zero (a timeout left by an earlier call would stop this one); the flags
-    // need no clearing, because a slot only matches this call's generation.
-    e = cudaMemsetAsync(scratch + kNoAllocFlagWords, 0, rr::kStatusWords * sizeof(uint32_t), stream);
+    // need no clearing, because a slot only passes for this call's generation.
+    uint32_t *status_words = scratch + kNoAllocFlagWords + kNoAllocRoundWords;
+    e = cudaMemsetAsync(status_words, 0, rr::kStatusWords * sizeof(uint32_t), stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status words)");
 
     rr::ReduceArgs a;
@@ -651,11 +721,17 @@ extern "C" rr_status rr_allreduce_oneshot_noalloc(const void *const *inputs, voi
     a.W = W;
     a.B = B;
     a.copy_mode = copy_mode ? 1 : 0;
+    {
+        const int64_t ng = (a.nvec + rr::kGranuleVec - 1) / rr::kGranuleVec;
+        a.round_vec = round_vectors(0, 4096, ((ng + B - 1) / B) * rr::kGranuleVec);
+    }
     a.sig.flags = scratch;
-    a.sig.status = scratch + kNoAllocFlagWords;
+    a.sig.rflags = reinterpret_cast<uint64_t *>(scratch + kNoAllocFlagWords);
+    a.sig.rbase = gen << rr::kRoundBits;
+    a.sig.status = status_words;
     a.sig.timeout_ns = rr::kDefaultTimeoutNs;
     a.sig.max_spins = (uint32_t)(rr::kDefaultTimeoutNs / 64 + 4096);
-    a.sig.g = gen;
+    a.sig.g = (uint32_t)gen;
     a.sig.W = W;
     a.sig.Bmax = kNoAllocMaxBlocks;
     a.sig.inject = -1;

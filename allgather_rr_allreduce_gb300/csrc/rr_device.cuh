@@ -56,15 +56,17 @@ __device__ __forceinline__ uint32_t *flag_slot(const SignalArgs &s, int listener
     return s.flags + idx;
 }
 
-// Publish "block b of rank r reached barrier `bar`" to every listener.  All
-// threads of the block call it; the CTA barrier orders every thread's earlier
-// writes before the release stores of lanes 0..W-1 of warp 0.
-__device__ __forceinline__ void emit(const SignalArgs &s, int bar, int r, int b)
+// Publish "block b of rank r reached barrier `bar`" to every listener by
+// storing `value` into its slot.  All threads of the block call it; the CTA
+// barrier orders every thread's earlier writes before the release stores of
+// lanes 0..W-1 of warp 0.
+__device__ __forceinline__ void emit(const SignalArgs &s, int bar, int r, int b, uint32_t value)
 {
     __syncthreads();
     if ((int)threadIdx.x < s.W && s.inject != r * kNumBarriers + bar)
-        st_flag_release(flag_slot(s, threadIdx.x, bar, b, r), s.g);
+        st_flag_release(flag_slot(s, threadIdx.x, bar, b, r), value);
 }
+__device__ __forceinline__ void emit(const SignalArgs &s, int bar, int r, int b) { emit(s, bar, r, b, s.g); }
 
 static __device__ __noinline__ void record_timeout(const SignalArgs &s, int bar, int r, int b)
 {
@@ -77,17 +79,28 @@ static __device__ __noinline__ void record_timeout(const SignalArgs &s, int bar,
     atomicExch(s.status + kStAbort, 1u);
 }
 
-// Warp 0 waits until every emitter's slot of (listener r, bar, block b) holds
-// this call's generation.  Lane p polls emitter p.  Bounded: gives up after
-// timeout_ns of %globaltimer, after max_spins polls, or as soon as the pad's
-// abort word is set (checked on the first poll and every 32nd after), and
-// then records the timeout.  Returns the same verdict to every thread.
-__device__ __forceinline__ bool wait(const SignalArgs &s, int bar, int r, int b, int *s_ok)
+// Warp 0 waits until every emitter's slot passes `seen_ok` (lane p polls
+// emitter p's slot).  Bounded: gives up after timeout_ns of %globaltimer,
+// after max_spins polls, or as soon as the pad's abort word is set (checked on
+// the first poll and every 32nd after), and then records the timeout against
+// barrier `bar`.  Returns the same verdict to every thread of the block.
+struct CtaSync {
+    __device__ void operator()() const { __syncthreads(); }
+};
+// Named barrier 1 over the first n threads (the consumer warps of a
+// warp-specialised block, while its producer warp runs on).
+struct GroupSync {
+    int n;
+    __device__ void operator()() const { asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory"); }
+};
+
+template <class Poll, class Sync = CtaSync>
+__device__ __forceinline__ bool wait_on(const SignalArgs &s, int bar, int r, int b, Poll poll, int *s_ok,
+                                        Sync sync = Sync())
 {
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
         const bool active = lane < s.W;
-        const uint32_t *slot = flag_slot(s, r, bar, b, active ? lane : 0);
         const uint64_t t0 = global_ns();
         bool seen = !active;
         bool ok = true;
@@ -96,7 +109,7 @@ __device__ __forceinline__ bool wait(const SignalArgs &s, int bar, int r, int b,
             uint32_t aborted = 0;
             const bool check = (spins & 31u) == 0u;
             if (check && lane == 0) aborted = ld_relaxed(s.status + kStAbort);
-            if (!seen) seen = ld_flag_acquire(slot) == s.g;
+            if (!seen) seen = poll(lane);
             const bool done = __all_sync(0xffffffffu, seen);
             if (check) {
                 const bool bad = aborted != 0u || spins > s.max_spins ||
@@ -115,8 +128,135 @@ __device__ __forceinline__ bool wait(const SignalArgs &s, int bar, int r, int b,
         if (!ok && lane == 0) record_timeout(s, bar, r, b);
         if (lane == 0) *s_ok = ok ? 1 : 0;
     }
-    __syncthreads();
+    sync();
     return *s_ok != 0;
+}
+
+// Call-level barrier: every emitter's slot of (listener r, bar, block b, this
+// call's parity) holds exactly this call's generation g.
+__device__ __forceinline__ bool wait(const SignalArgs &s, int bar, int r, int b, int *s_ok)
+{
+    const uint32_t *slots = flag_slot(s, r, bar, b, 0);
+    return wait_on(s, bar, r, b, [&](int p) { return ld_flag_acquire(slots + p) == s.g; }, s_ok);
+}
+
+// ------------------------------------------------------------ round flags
+// A barrier passed once per round of a pipelined chunk (staging, the two-shot
+// middle) stores increasing 64-bit values, rbase + k + 1 for round k, where
+// rbase = (64-bit call generation) << kRoundBits; a wait accepts any value at
+// or past its target.  Values only grow, so no parity halves are needed, an
+// emitter may run ahead by several rounds, and a stale value from an earlier
+// call is always below the target (no wrap-around in 2^48 calls).
+__device__ __forceinline__ void st_flag64_release(uint64_t *p, uint64_t v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_flag64_acquire(const uint64_t *p)
+{
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint64_t *round_slot(const SignalArgs &s, int listener, int kind, int b, int emitter)
+{
+    return s.rflags + ((((size_t)listener * kRoundKinds + kind) * (size_t)s.Bmax + b) * (size_t)s.W + emitter);
+}
+// kind 0 = staging (reported as RR_BARRIER_STAGE), 1 = two-shot middle (RR_BARRIER_MID)
+__device__ __forceinline__ int round_barrier(int kind) { return kind == 0 ? RR_BARRIER_STAGE : RR_BARRIER_MID; }
+
+__device__ __forceinline__ void emit_round(const SignalArgs &s, int kind, int r, int b, int k)
+{
+    __syncthreads();
+    if ((int)threadIdx.x < s.W && s.inject != r * kNumBarriers + round_barrier(kind))
+        st_flag64_release(round_slot(s, threadIdx.x, kind, b, r), s.rbase + (uint64_t)k + 1u);
+}
+template <class Sync = CtaSync>
+__device__ __forceinline__ bool wait_round(const SignalArgs &s, int kind, int r, int b, int k, int *s_ok,
+                                           Sync sync = Sync())
+{
+    const uint64_t *slots = round_slot(s, r, kind, b, 0);
+    const uint64_t target = s.rbase + (uint64_t)k + 1u;
+    return wait_on(s, round_barrier(kind), r, b,
+                   [&](int p) { return (int64_t)(ld_flag64_acquire(slots + p) - target) >= 0; }, s_ok, sync);
+}
+// Round flag k from a single thread (the producer lane of a warp-specialised
+// block): stores to all W listeners.  The caller has made the round's data
+// visible (bulk-store completion and an async-proxy fence).
+__device__ __forceinline__ void emit_round_single(const SignalArgs &s, int kind, int r, int b, int k)
+{
+    if (s.inject == r * kNumBarriers + round_barrier(kind)) return;
+    for (int p = 0; p < s.W; ++p) st_flag64_release(round_slot(s, p, kind, b, r), s.rbase + (uint64_t)k + 1u);
+}
+
+// ------------------------------------------------------------ bulk copies
+// cp.async.bulk (TMA without a tensor map) between global and shared memory,
+// completion of loads counted on an mbarrier, stores tracked in bulk groups.
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(sdst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// At most N bulk groups still incomplete (the older ones' writes have landed).
+template <int N>
+__device__ __forceinline__ void bulk_wait_pending() { asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Bounded wait for an mbarrier phase: false after the pad's timeout or
+// iteration limit (the caller records the failure and stops).
+__device__ __forceinline__ bool mbar_wait_bounded(const SignalArgs &s, uint64_t *bar, uint32_t parity)
+{
+    const uint64_t t0 = global_ns();
+    for (uint32_t spins = 0; !mbar_try_wait(bar, parity); ++spins) {
+        if ((spins & 255u) == 255u && ((global_ns() - t0) > s.timeout_ns || spins > s.max_spins))
+            return false;
+    }
+    return true;
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // ---------------------------------------------------------------- arithmetic

@@ -16,6 +16,8 @@
 namespace rr {
 
 constexpr int kNumBarriers = 4;       // rr_barrier values
+constexpr int kRoundKinds = 2;        // barriers passed once per round: STAGE, MID
+constexpr int kRoundBits = 16;        // rounds per call < 2^16
 constexpr int kDefaultMaxBlocks = 1024;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
@@ -33,6 +35,8 @@ enum StatusWord : int {
 // Everything a kernel needs to take part in the pad's barriers.
 struct SignalArgs {
     uint32_t *flags;     // [W listener][kNumBarriers][2][Bmax][W emitter]
+    uint64_t *rflags;    // [W listener][kRoundKinds][Bmax][W emitter], round flags
+    uint64_t rbase;      // this call's 64-bit generation << kRoundBits
     uint32_t *status;    // kStatusWords words
     uint64_t timeout_ns; // per wait
     uint32_t max_spins;  // iteration backstop of a wait, in case the timer misbehaves
@@ -49,6 +53,7 @@ struct ReduceArgs {
     void *out[RR_MAX_WORLD];       // outputs (may be null for one-shot)
     int64_t numel;                 // elements per rank
     int64_t nvec;                  // whole 16-byte vectors per rank
+    int64_t round_vec;             // vectors per round of a pipelined chunk (multiple of 16)
     int W;
     int B;                         // blocks per rank
     int copy_mode;
@@ -129,9 +134,13 @@ struct KernelChoice {
     const void *fn;
     int threads;
     int smem;
+    int per_sm = 0;  // preferred resident blocks per SM for large messages (0 = as many as fit)
 };
-KernelChoice oneshot_kernel_for(rr_dtype dtype, int W);
-KernelChoice twoshot_kernel_for(rr_dtype dtype, int W);
+KernelChoice oneshot_kernel_for(rr_dtype dtype, int W, bool copy_mode);
+KernelChoice twoshot_kernel_for(rr_dtype dtype, int W, bool copy_mode, bool push);
+KernelChoice oneshot_tma_kernel_for(rr_dtype dtype, int W);  // copy_mode off, bulk-copy loads
+// copy_mode on, staging by a bulk-copy producer warp (two-shot: push allgather)
+KernelChoice staged_kernel_for(rr_dtype dtype, int W, bool twoshot);
 KernelChoice gather_kernel_for(int engine);  // 1 = loads/stores, 2 = TMA bulk
 
 }  // namespace rr

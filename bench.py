@@ -226,12 +226,15 @@ class Step:
         }
         return {op: full[op] for op in self.ops}
 
-    def run(self, events=None):
+    def run(self, events=None, only=None):
+        """One step.  events[i] = (start, end) pair recorded around op i
+        (every op, or only op index `only`)."""
         for i, name in enumerate(self.ops):
-            if events is not None:
+            timed = events is not None and (only is None or i == only)
+            if timed:
                 events[i][0].record(self.stream)
             self.calls[name]()
-            if events is not None:
+            if timed:
                 events[i][1].record(self.stream)
 
     def run_e2e(self):
@@ -339,34 +342,56 @@ def run_gpu(args, rank, world, local_rank):
     ops = tuple(args.only.split(",")) if args.only else OP_NAMES
     step = Step(rr, stream, seed=workloads.LARGE["seed_base"] + 97 * rank, ops=ops,
                 n=args.numel or N, pc_div=args.pc_div)
+    step.pad.set_option("reduce_engine", ("auto", "ldst", "tma").index(args.reduce_engine))
+    step.pad.set_option("twoshot_mode", ("auto", "pull", "push").index(args.twoshot_mode))
     bytes_by_op = step.bytes_by_op()
     step_bytes = sum(bytes_by_op.values())
     torch.cuda.synchronize()
 
+    def new_events():
+        return [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in ops]
+
+    def op_ms(evs, i):
+        return [e[i][0].elapsed_time(e[i][1]) for e in evs]
+
     sampler = ClockSampler(local_rank)
     if rank == 0:
         sampler.start()
-    for _ in range(args.warmup):
-        step.run()
+    # Warm-up, with an event pair around every op: picks the op with the
+    # largest share of the step (the roofline kernel).
+    warm = [new_events() for _ in range(args.warmup)]
+    for k in range(args.warmup):
+        step.run(warm[k])
     stream.synchronize()
+    tail = warm[max(1, args.warmup // 2):] or warm
+    dom_i = max(range(len(ops)), key=lambda i: statistics.mean(op_ms(tail, i)))
 
-    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in ops]
-              for _ in range(args.steps)]
+    # Timed region: exactly K steps; events only around the roofline op (an
+    # event pair between two launches costs a few microseconds, so none are
+    # put around the other ops here).
+    events = [new_events() for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     t_start.record(stream)
     for k in range(args.steps):
-        step.run(events[k])
+        step.run(events[k], only=dom_i)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop() if rank == 0 else None
     step.pad.status(stream)
     elapsed_ms = t_start.elapsed_time(t_end)
-    per_op_ms = {name: [events[k][i][0].elapsed_time(events[k][i][1]) for k in range(args.steps)]
-                 for i, name in enumerate(ops)}
+    dom_ms = op_ms(events, dom_i)
+
+    # Per-op breakdown, after the timed region: event pairs around every op.
+    n_prof = min(args.steps, 100)
+    prof = [new_events() for _ in range(n_prof)]
+    for k in range(n_prof):
+        step.run(prof[k])
+    stream.synchronize()
+    per_op_ms = {name: op_ms(prof, i) for i, name in enumerate(ops)}
 
     max_ms = max_over_ranks(elapsed_ms, world)
 
@@ -399,9 +424,8 @@ def run_gpu(args, rank, world, local_rank):
                      "us_median": round(1000 * statistics.median(per_op_ms[name]), 2),
                      "GBps": round(gbs, 1), "pct_of_8TBps": round(100 * gbs / NOMINAL_HBM_GBS, 2),
                      f"frac_of_{peak_kind}": round(gbs / peak, 4)}
-    dominant = max(ops, key=lambda n: op_stats[n]["us"])
-    step_bytes = sum(bytes_by_op.values())
-    dom = op_stats[dominant]
+    dominant = ops[dom_i]
+    dom_gbs = bytes_by_op[dominant] / statistics.mean(dom_ms) / 1e6
     ms_per_step = max_ms / args.steps
     value = world * step_bytes / ms_per_step / 1e6
 
@@ -424,14 +448,18 @@ def run_gpu(args, rank, world, local_rank):
         "dtype": "bf16",
         "data": "synthetic (seeded torch RNG on the device; N(0,1) ranks, N(0,0.02) layer shards)",
         "config": {"workload": workload_name(ops, step.n, args.pc_div),
+                   "reduce_engine": args.reduce_engine, "twoshot_mode": args.twoshot_mode,
                    "W": W, "numel_per_rank": step.n, "bytes_per_step": step_bytes,
                    "l2": "inputs larger than L2 (every op >= 288 MiB of its own buffers; L2 129 MB)",
                    "parallelism": f"replicas x{world} (no inter-GPU collective; W ranks emulated per GPU)"},
-        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": dom["GBps"], "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(dom_gbs, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs (STREAM-style copy, burst)", "unit": "GB/s",
-                     "frac": round(dom["GBps"] / peak, 4), "traffic": recorded_traffic(dominant),
+                     "frac": round(dom_gbs / peak, 4), "traffic": recorded_traffic(dominant),
+                     "us_per_launch": round(1000 * statistics.mean(dom_ms), 2),
                      "algorithmic_bytes_per_launch": bytes_by_op[dominant]},
         "ops": op_stats,
+        "ops_note": f"per-op breakdown from {n_prof} extra steps with an event pair around every op "
+                    "(each pair adds a few us to its op); value uses the timed steps",
         "e2e": {"value": round(world * step_bytes / e2e_ms / 1e6, 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
         "gpu_launches": len(ops) * args.steps,
@@ -541,6 +569,10 @@ def main():
     ap.add_argument("--only", default="", help="comma-separated subset of ops (profiling runs)")
     ap.add_argument("--numel", type=int, default=0, help="elements per rank for the allreduce/allgather ops")
     ap.add_argument("--pc-div", type=int, default=1, help="divide the FSDP layer's splits by this")
+    ap.add_argument("--reduce-engine", choices=("auto", "ldst", "tma"), default="auto",
+                    help="allreduce engine (pad option reduce_engine)")
+    ap.add_argument("--twoshot-mode", choices=("auto", "pull", "push"), default="auto",
+                    help="two-shot allgather phase (pad option twoshot_mode)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

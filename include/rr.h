@@ -81,11 +81,23 @@ typedef enum {
     RR_OPT_GATHER_ENGINE = 2,   /* 0 = automatic, 1 = 128-bit loads/stores, 2 = TMA bulk copies */
     RR_OPT_INJECT_SKIP = 3,     /* fault injection: -1 = off; else rank*4 + barrier: that rank
                                    never emits that barrier's flags, so peers time out */
+    RR_OPT_ROUND_BYTES = 4,     /* bytes per rank per round of a pipelined chunk (copy_mode
+                                   staging, two-shot); 0 = automatic (64 KiB one-shot,
+                                   32 KiB two-shot) */
+    RR_OPT_REDUCE_ENGINE = 5,   /* 0 = automatic, 1 = 128-bit loads/stores, 2 = bulk-copy (TMA)
+                                   engine: copy_mode off, the one-shot's loads stream into a
+                                   shared-memory ring; copy_mode on, a producer warp stages the
+                                   inputs by bulk copies while the other warps reduce (the
+                                   two-shot then uses the push allgather) */
+    RR_OPT_TWOSHOT_MODE = 6,    /* two-shot allgather phase: 0 = automatic (push), 1 = pull (every rank
+                                   copies the other owners' reduced chunks after the MID
+                                   barrier), 2 = push (each owner stores its reduced chunk into
+                                   every output; no MID barrier) */
     /* read-only */
     RR_OPT_GENERATION = 16,     /* generation flag value of the last call */
     RR_OPT_LAST_GRID = 17,      /* blocks launched by the last call */
     RR_OPT_LAST_BLOCKS_PER_RANK = 18,
-    RR_OPT_LAST_ENGINE = 19,    /* engine the last gather used (1 or 2) */
+    RR_OPT_LAST_ENGINE = 19,    /* engine the last call used (1 = loads/stores, 2 = bulk copies) */
     RR_OPT_WORLD_SIZE = 20,
     RR_OPT_MAX_BLOCKS_PER_RANK = 21
 } rr_option;
@@ -100,10 +112,14 @@ typedef struct rr_signal_pad rr_signal_pad; /* opaque, owned by the library */
  * in "Question and suggestions about custom allreduce" (sglang discussion
  * 2918), leizhao1234's first post: dimension 0 listens, the last dimension
  * emits.  Layout here: [W listener][4 barriers][2 parities][blocks][W emitter]
- * uint32 words on the current device, plus a status block.  Each call takes
- * the next generation value g (a host counter, never 0) and writes g into
- * slots of parity g & 1, so consecutive calls never share a slot (the same
- * post picks the half of the arrival flags to use from the flag's parity).
+ * uint32 words on the current device, then [W listener][2][blocks][W emitter]
+ * uint64 round flags, then a status block.  Each call takes the next
+ * generation value g (a host counter, never 0) and writes g into slots of
+ * parity g & 1, so consecutive calls never share a slot (the same post picks
+ * the half of the arrival flags to use from the flag's parity).  Barriers
+ * passed once per round of a pipelined chunk (copy_mode staging, the two-shot
+ * middle) use the 64-bit round flags instead: values that only grow, from a
+ * 64-bit call counter, waited on as "at least".
  *
  * world_size: W, 1..RR_MAX_WORLD.  max_blocks_per_rank: upper bound on
  * blocks per rank any call on this pad may use (0 = 1024).  timeout_ns:
@@ -247,7 +263,7 @@ rr_status rr_allgather_param_contiguous(const void *const *rank_bufs, void *cons
  * device synchronisation would stall the GPU.  Those callers cannot create a
  * signal pad (rr_signal_pad_create calls cudaMalloc).  This call uses instead
  * a fixed signal pad that the library holds in a static device array of
- * 64 KiB + 32 bytes, present on every GPU that loads the library until the
+ * 96 KiB + 32 bytes, present on every GPU that loads the library until the
  * process exits.  It calls no cudaMalloc, cudaFree or allocating routine.
  *
  * Arguments, results and errors are those of rr_allreduce_oneshot without

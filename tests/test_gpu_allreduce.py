@@ -54,9 +54,14 @@ def run_allreduce(rr, algo, W, N, dtype, copy_mode, ins, materialise=None, layou
         bufs.fill(ins)
     outs = GuardedOutputs(W, N, dtype, materialise=materialise)
     fn = rr.rr_allreduce_oneshot if algo == "oneshot" else rr.rr_allreduce_twoshot
-    fn(src.ptrs if copy_mode else None, bufs.ptrs, outs.ptrs, W, N, dtype, copy_mode, pad)
-    pad.status()
-    pad.set_option("blocks_per_rank", 0)
+    if algo == "twoshot_pull":
+        pad.set_option("twoshot_mode", 1)
+    try:
+        fn(src.ptrs if copy_mode else None, bufs.ptrs, outs.ptrs, W, N, dtype, copy_mode, pad)
+        pad.status()
+    finally:
+        pad.set_option("twoshot_mode", 0)
+        pad.set_option("blocks_per_rank", 0)
     return bufs, src, outs
 
 
@@ -64,7 +69,7 @@ SHAPES = [(2, 4096), (1, 100), (2, 4099), (3, 12345), (4, 1), (5, 8 * 16 * 33 + 
           (16, 10000), (7, 3)]
 
 
-@pytest.mark.parametrize("algo", ["oneshot", "twoshot"])
+@pytest.mark.parametrize("algo", ["oneshot", "twoshot", "twoshot_pull"])
 @pytest.mark.parametrize("copy_mode", [0, 1])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32", "int32"])
 @pytest.mark.parametrize("W,N", SHAPES, ids=[f"W{w}_N{n}" for w, n in SHAPES])
@@ -106,7 +111,7 @@ def test_oneshot_subset_of_outputs(rr, materialise, copy_mode):
 
 
 @pytest.mark.parametrize("blocks", [1, 2, 7, 64])
-@pytest.mark.parametrize("algo", ["oneshot", "twoshot"])
+@pytest.mark.parametrize("algo", ["oneshot", "twoshot", "twoshot_pull"])
 def test_fixed_blocks_per_rank(rr, blocks, algo):
     """The result does not depend on how many blocks each rank runs,
     including the single-block degenerate case."""
@@ -117,6 +122,141 @@ def test_fixed_blocks_per_rank(rr, blocks, algo):
         _, _, outs = run_allreduce(rr, algo, W, N, dtype, copy_mode, ins, blocks_per_rank=blocks)
         for r in range(W):
             assert_bitwise(outs.host(r), want, f"{algo} blocks={blocks} output {r}")
+
+
+@pytest.mark.parametrize("round_bytes", [256, 4096, 1 << 20])
+@pytest.mark.parametrize("algo", ["oneshot", "twoshot", "twoshot_pull"])
+@pytest.mark.parametrize("copy_mode", [0, 1])
+def test_round_sizes(rr, round_bytes, algo, copy_mode):
+    """The pipelined chunk gives the same bits with 16-vector rounds (many
+    rounds per block), the default, and one round per block."""
+    W, N, dtype = 8, 3 * (1 << 17) + 11, "bf16"
+    ins = workloads.rank_buffers(W, N, dtype, "normal", seed_base=21)
+    want = oracle.allreduce(ins, dtype)
+    pad = pad_for(rr, W)
+    pad.set_option("round_bytes", round_bytes)
+    try:
+        _, _, outs = run_allreduce(rr, algo, W, N, dtype, copy_mode, ins,
+                                   materialise=None if algo != "oneshot" else (0, 6))
+    finally:
+        pad.set_option("round_bytes", 0)
+    for r in (range(W) if algo != "oneshot" else (0, 6)):
+        assert_bitwise(outs.host(r), want, f"{algo} round_bytes={round_bytes} output {r}")
+    outs.check_guards()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32", "int32"])
+@pytest.mark.parametrize("W,N", SHAPES + [(8, (1 << 20) + 3)], ids=[f"W{w}_N{n}" for w, n in SHAPES + [(8, (1 << 20) + 3)]])
+def test_oneshot_tma_engine_matches_oracle(rr, dtype, W, N):
+    """The one-shot with bulk-copy (TMA) loads, every output kept and rank 0
+    only: same bits as the oracle."""
+    ins = workloads.rank_buffers(W, N, dtype, dist_for(dtype), seed_base=300 * W + N % 89)
+    want = oracle.allreduce(ins, dtype)
+    pad = pad_for(rr, W)
+    pad.set_option("reduce_engine", 2)
+    try:
+        for materialise in (None, (0,)):
+            _, _, outs = run_allreduce(rr, "oneshot", W, N, dtype, 0, ins, materialise=materialise)
+            assert pad.get_option("last_engine") == 2
+            for r in (range(W) if materialise is None else materialise):
+                assert_bitwise(outs.host(r), want, f"tma engine output {r}")
+            outs.check_guards()
+    finally:
+        pad.set_option("reduce_engine", 0)
+
+
+@pytest.mark.parametrize("blocks", [1, 3, 16])
+def test_oneshot_tma_engine_fixed_blocks(rr, blocks):
+    W, N, dtype = 4, 300_001, "bf16"
+    ins = workloads.rank_buffers(W, N, dtype, "normal", seed_base=19)
+    want = oracle.allreduce(ins, dtype)
+    pad = pad_for(rr, W)
+    pad.set_option("reduce_engine", 2)
+    try:
+        _, _, outs = run_allreduce(rr, "oneshot", W, N, dtype, 0, ins, materialise=(1, 2),
+                                   blocks_per_rank=blocks)
+    finally:
+        pad.set_option("reduce_engine", 0)
+    for r in (1, 2):
+        assert_bitwise(outs.host(r), want)
+
+
+@pytest.mark.parametrize("copy_mode", [0, 1])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32", "int32"])
+@pytest.mark.parametrize("W,N", SHAPES + [(8, (1 << 20) + 3)], ids=[f"W{w}_N{n}" for w, n in SHAPES + [(8, (1 << 20) + 3)]])
+def test_twoshot_push_mode_matches_oracle(rr, copy_mode, dtype, W, N):
+    """Two-shot whose allgather is a broadcast by each chunk's owner."""
+    ins = workloads.rank_buffers(W, N, dtype, dist_for(dtype), seed_base=700 * W + N % 83)
+    want = oracle.allreduce(ins, dtype)
+    pad = pad_for(rr, W)
+    pad.set_option("twoshot_mode", 2)
+    try:
+        bufs, src, outs = run_allreduce(rr, "twoshot", W, N, dtype, copy_mode, ins)
+    finally:
+        pad.set_option("twoshot_mode", 0)
+    for r in range(W):
+        assert_bitwise(outs.host(r), want, f"push output {r}")
+    outs.check_guards()
+    for r in range(W):
+        assert_bitwise(bufs.host(r), ins[r])
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("blocks", [1, 5])
+def test_twoshot_modes_fixed_blocks(rr, mode, blocks):
+    W, N, dtype = 8, 500_009, "bf16"
+    ins = workloads.rank_buffers(W, N, dtype, "normal", seed_base=23)
+    want = oracle.allreduce(ins, dtype)
+    pad = pad_for(rr, W)
+    pad.set_option("twoshot_mode", mode)
+    try:
+        for copy_mode in (0, 1):
+            _, _, outs = run_allreduce(rr, "twoshot", W, N, dtype, copy_mode, ins, blocks_per_rank=blocks)
+            for r in range(W):
+                assert_bitwise(outs.host(r), want)
+    finally:
+        pad.set_option("twoshot_mode", 0)
+
+
+@pytest.mark.parametrize("algo", ["oneshot", "twoshot"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32", "int32"])
+@pytest.mark.parametrize("W,N", SHAPES + [(8, (1 << 20) + 3)], ids=[f"W{w}_N{n}" for w, n in SHAPES + [(8, (1 << 20) + 3)]])
+def test_staged_copy_mode_matches_oracle(rr, algo, dtype, W, N):
+    """copy_mode with the staging done by a bulk-copy producer warp."""
+    ins = workloads.rank_buffers(W, N, dtype, dist_for(dtype), seed_base=900 * W + N % 79)
+    want = oracle.allreduce(ins, dtype)
+    pad = pad_for(rr, W)
+    pad.set_option("reduce_engine", 2)
+    try:
+        for materialise in ((None,) if algo == "twoshot" else (None, (0,))):
+            bufs, src, outs = run_allreduce(rr, algo, W, N, dtype, 1, ins, materialise=materialise)
+            assert pad.get_option("last_engine") == 2
+            for r in (range(W) if materialise is None else materialise):
+                assert_bitwise(outs.host(r), want, f"staged {algo} output {r}")
+            outs.check_guards()
+            for r in range(W):
+                assert_bitwise(bufs.host(r), ins[r], f"staged rank buffer {r}")
+    finally:
+        pad.set_option("reduce_engine", 0)
+
+
+@pytest.mark.parametrize("round_bytes", [256, 16384, 1 << 22])
+@pytest.mark.parametrize("blocks", [1, 3, 19])
+@pytest.mark.parametrize("algo", ["oneshot", "twoshot"])
+def test_staged_rounds_and_blocks(rr, round_bytes, blocks, algo):
+    W, N, dtype = 8, 3 * (1 << 18) + 5, "bf16"
+    ins = workloads.rank_buffers(W, N, dtype, "normal", seed_base=29)
+    want = oracle.allreduce(ins, dtype)
+    pad = pad_for(rr, W)
+    pad.set_option("reduce_engine", 2)
+    pad.set_option("round_bytes", round_bytes)
+    try:
+        _, _, outs = run_allreduce(rr, algo, W, N, dtype, 1, ins, blocks_per_rank=blocks)
+    finally:
+        pad.set_option("reduce_engine", 0)
+        pad.set_option("round_bytes", 0)
+    for r in range(W):
+        assert_bitwise(outs.host(r), want, f"{algo} round_bytes={round_bytes} blocks={blocks} output {r}")
 
 
 def test_separate_allocations(rr):
@@ -155,14 +295,14 @@ def test_twoshot_equals_oneshot_repeated(rr):
     ins = workloads.rank_buffers(W, N, dtype, "normal", seed_base=13)
     _, _, a = run_allreduce(rr, "oneshot", W, N, dtype, 0, ins)
     first = a.host(0)
-    for algo in ("twoshot", "oneshot", "twoshot"):
+    for algo in ("twoshot", "oneshot", "twoshot_pull"):
         for copy_mode in (0, 1):
             _, _, o = run_allreduce(rr, algo, W, N, dtype, copy_mode, ins)
             for r in range(W):
                 assert_bitwise(o.host(r), first, f"{algo} copy={copy_mode} rank {r}")
 
 
-@pytest.mark.parametrize("algo", ["oneshot", "twoshot"])
+@pytest.mark.parametrize("algo", ["oneshot", "twoshot", "twoshot_pull"])
 @pytest.mark.parametrize("copy_mode", [0, 1])
 def test_large_workload_full(rr, algo, copy_mode):
     """W=8, bf16, 2^24 elements (32 MiB) per rank, N(0, 1): every output
@@ -177,7 +317,7 @@ def test_large_workload_full(rr, algo, copy_mode):
     outs.check_guards()
 
 
-@pytest.mark.parametrize("algo", ["oneshot", "twoshot"])
+@pytest.mark.parametrize("algo", ["oneshot", "twoshot", "twoshot_pull"])
 @pytest.mark.parametrize("copy_mode", [0, 1])
 @pytest.mark.parametrize("kib", [8, 64, 256])
 def test_back_to_back_alternating_inputs(rr, algo, copy_mode, kib):
@@ -199,6 +339,7 @@ def test_back_to_back_alternating_inputs(rr, algo, copy_mode, kib):
     outs = torch.empty((calls, W, N), dtype=torch.bfloat16, device="cuda")
     fn = rr.rr_allreduce_oneshot if algo == "oneshot" else rr.rr_allreduce_twoshot
     stream = torch.cuda.current_stream()
+    pad.set_option("twoshot_mode", 1 if algo == "twoshot_pull" else 0)
     for i in range(calls):
         s = srcs[i % 2]
         optrs = [outs[i, r].data_ptr() for r in range(W)]
@@ -207,6 +348,7 @@ def test_back_to_back_alternating_inputs(rr, algo, copy_mode, kib):
         else:
             fn(None, s.ptrs, optrs, W, N, dtype, 0, pad, stream)
     pad.status(stream)
+    pad.set_option("twoshot_mode", 0)
     for i in range(calls):
         w = wants[i % 2]
         for r in range(W):

@@ -38,14 +38,16 @@ def _call(rr, algo, pad, W, N, ins, copy_mode):
     src = RankBuffers(W, N, "bf16")
     (src if copy_mode else bufs).fill(ins)
     outs = GuardedOutputs(W, N, "bf16")
-    fn = {"oneshot": rr.rr_allreduce_oneshot, "twoshot": rr.rr_allreduce_twoshot}[algo]
+    fn = rr.rr_allreduce_oneshot if algo == "oneshot" else rr.rr_allreduce_twoshot
+    pad.set_option("twoshot_mode", 1 if algo == "twoshot_pull" else 0)
     fn(src.ptrs if copy_mode else None, bufs.ptrs, outs.ptrs, W, N, "bf16", copy_mode, pad)
+    pad.set_option("twoshot_mode", 0)
     return outs
 
 
 CASES = [
     ("oneshot", 0, 1, "ARRIVE"), ("oneshot", 1, 2, "STAGE"), ("oneshot", 0, 3, "END"),
-    ("twoshot", 0, 0, "MID"), ("twoshot", 1, 1, "STAGE"), ("twoshot", 1, 2, "END"),
+    ("twoshot_pull", 0, 0, "MID"), ("twoshot_pull", 1, 1, "STAGE"), ("twoshot_pull", 1, 2, "END"),
 ]
 
 
@@ -70,6 +72,63 @@ def test_skipped_flag_times_out_and_recovers(rr, algo, copy_mode, rank, barrier)
     pad.status()
     for r in range(W):
         assert_bitwise(outs.host(r), want, f"after recovery, output {r}")
+    pad.close()
+
+
+def test_tma_oneshot_times_out_and_recovers(rr):
+    W, N = 4, 200_000
+    ins, want = _inputs(W, N)
+    pad = rr.rr_signal_pad_create(W, 0, SHORT_NS)
+    pad.set_option("reduce_engine", 2)
+    for rank, barrier in ((2, "ARRIVE"), (1, "END")):
+        pad.set_option("inject_skip", rank * 4 + getattr(rr, f"RR_BARRIER_{barrier}"))
+        _call(rr, "oneshot", pad, W, N, ins, 0)
+        with pytest.raises(rr.RRError) as e:
+            pad.status()
+        assert e.value.status == rr.RR_ERR_TIMEOUT
+        pad.set_option("inject_skip", -1)
+        outs = _call(rr, "oneshot", pad, W, N, ins, 0)
+        pad.status()
+        for r in range(W):
+            assert_bitwise(outs.host(r), want)
+    pad.close()
+
+
+@pytest.mark.parametrize("copy_mode,barrier", [(0, "END"), (1, "STAGE"), (0, "ARRIVE")])
+def test_twoshot_push_times_out_and_recovers(rr, copy_mode, barrier):
+    W, N = 4, 60_000
+    ins, want = _inputs(W, N)
+    pad = rr.rr_signal_pad_create(W, 0, SHORT_NS)
+    pad.set_option("twoshot_mode", 2)
+    pad.set_option("inject_skip", 3 * 4 + getattr(rr, f"RR_BARRIER_{barrier}"))
+    _call(rr, "twoshot", pad, W, N, ins, copy_mode)
+    with pytest.raises(rr.RRError) as e:
+        pad.status()
+    assert e.value.status == rr.RR_ERR_TIMEOUT
+    pad.set_option("inject_skip", -1)
+    outs = _call(rr, "twoshot", pad, W, N, ins, copy_mode)
+    pad.status()
+    for r in range(W):
+        assert_bitwise(outs.host(r), want)
+    pad.close()
+
+
+@pytest.mark.parametrize("algo,barrier", [("oneshot", "STAGE"), ("twoshot", "STAGE"), ("oneshot", "END")])
+def test_staged_copy_mode_times_out_and_recovers(rr, algo, barrier):
+    W, N = 4, 300_000
+    ins, want = _inputs(W, N)
+    pad = rr.rr_signal_pad_create(W, 0, SHORT_NS)
+    pad.set_option("reduce_engine", 2)
+    pad.set_option("inject_skip", 1 * 4 + getattr(rr, f"RR_BARRIER_{barrier}"))
+    _call(rr, algo, pad, W, N, ins, 1)
+    with pytest.raises(rr.RRError) as e:
+        pad.status()
+    assert e.value.status == rr.RR_ERR_TIMEOUT
+    pad.set_option("inject_skip", -1)
+    outs = _call(rr, algo, pad, W, N, ins, 1)
+    pad.status()
+    for r in range(W):
+        assert_bitwise(outs.host(r), want)
     pad.close()
 
 
@@ -121,8 +180,8 @@ def test_generation_advances_and_keeps_parity(rr):
     ins, want = _inputs(W, N)
     pad = rr.rr_signal_pad_create(W)
     g0 = pad.get_option("generation")
-    for k in range(5):
-        outs = _call(rr, "twoshot", pad, W, N, ins, k % 2)
+    for k in range(6):
+        outs = _call(rr, ("twoshot", "twoshot_pull", "oneshot")[k % 3], pad, W, N, ins, k % 2)
         assert pad.get_option("generation") == g0 + k + 1
     pad.status()
     assert_bitwise(outs.host(1), want)
