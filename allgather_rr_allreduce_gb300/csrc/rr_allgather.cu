@@ -101,13 +101,13 @@ __device__ __forceinline__ void push_bytes(const GatherArgs &a, const char *src,
 }
 
 // ------------------------------------------------------------------ ldst engine
-__global__ void __launch_bounds__(kLdstThreads) gather_kernel_ldst(const __grid_constant__ GatherArgs a)
+__device__ __forceinline__ void gather_kernel_ldst_body(const GatherArgs &a, const SignalArgs &sig)
 {
     __shared__ int s_ok;
     const int r = blockIdx.x / a.B;
     const int b = blockIdx.x - r * a.B;
-    if (b == 0) emit(a.sig, RR_BARRIER_ARRIVE, r, 0);
-    if (!wait(a.sig, RR_BARRIER_ARRIVE, r, 0, &s_ok)) return;
+    if (b == 0) emit(sig, RR_BARRIER_ARRIVE, r, 0);
+    if (!wait(sig, RR_BARRIER_ARRIVE, r, 0, &s_ok)) return;
 
     int64_t x0, x1;
     byte_region(a.off[a.nsplit], a.B, b, x0, x1);
@@ -119,8 +119,15 @@ __global__ void __launch_bounds__(kLdstThreads) gather_kernel_ldst(const __grid_
                 push_bytes(a, src + p0, d0, p1 - p0, threadIdx.x, kLdstThreads);
         }
     }
-    emit(a.sig, RR_BARRIER_END, r, b);
-    wait(a.sig, RR_BARRIER_END, r, b, &s_ok);
+    emit(sig, RR_BARRIER_END, r, b);
+    wait(sig, RR_BARRIER_END, r, b, &s_ok);
+}
+
+__global__ void __launch_bounds__(kLdstThreads) gather_kernel_ldst(const __grid_constant__ GatherArgs a)
+{
+    const SignalArgs sig = begin_call(a.sig);
+    gather_kernel_ldst_body(a, sig);
+    end_call(sig);
 }
 
 // ------------------------------------------------------------------ tma engine
@@ -135,85 +142,92 @@ __device__ __forceinline__ bool bulk_part(const GatherArgs &a, int r, int s, int
     return pend > p0;
 }
 
-
-__global__ void __launch_bounds__(kTmaThreads) gather_kernel_tma(const __grid_constant__ GatherArgs a)
+__device__ __forceinline__ void gather_kernel_tma_body(const GatherArgs &a, const SignalArgs &sig)
 {
     extern __shared__ __align__(128) unsigned char stage_mem[];
     __shared__ __align__(8) uint64_t full[kTmaStages];
     __shared__ int s_ok;
     const int r = blockIdx.x / a.B;
     const int b = blockIdx.x - r * a.B;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kTmaStages; ++i) mbar_init(&full[i], 1);
-        fence_mbar_init();
-    }
-    if (b == 0) emit(a.sig, RR_BARRIER_ARRIVE, r, 0);
-    else __syncthreads();
-    if (!wait(a.sig, RR_BARRIER_ARRIVE, r, 0, &s_ok)) return;
-
     int64_t x0, x1;
     byte_region(a.off[a.nsplit], a.B, b, x0, x1);
     const char *src = static_cast<const char *>(a.src[r]);
     const int sfirst = x0 < x1 ? first_split_after(a, x0) : a.nsplit;
 
+    // Chunk iterator over the bulk parts of the region's pieces (thread 0).
+    int s = sfirst - 1;
+    int64_t pos = 0, pend = 0, dpos = 0;
+    auto next = [&](int64_t &cs, int64_t &cd, uint32_t &cl) -> bool {
+        while (pos >= pend) {
+            ++s;
+            if (s >= a.nsplit || a.off[s] >= x1) return false;
+            int64_t p0, pe, d0;
+            if (bulk_part(a, r, s, x0, x1, p0, pe, d0)) {
+                pos = p0;
+                pend = pe;
+                dpos = d0;
+            }
+        }
+        const int64_t left = pend - pos;
+        cl = (uint32_t)(left < kTmaChunk ? left : kTmaChunk);
+        cs = pos;
+        cd = dpos;
+        pos += cl;
+        dpos += cl;
+        return true;
+    };
+    int64_t dst_of[kTmaStages];
+    uint32_t len_of[kTmaStages];
+    auto issue = [&](int k, int64_t cs, int64_t cd, uint32_t cl) {
+        const int st = k % kTmaStages;
+        dst_of[st] = cd;
+        len_of[st] = cl;
+        mbar_expect_tx(&full[st], cl);
+        bulk_load(stage_mem + (size_t)st * kTmaChunk, src + cs, cl, &full[st]);
+    };
+    auto drain = [&](int from, int to) {
+        // Let loads already in flight land before this block's shared
+        // memory can be handed to anyone else.
+        for (int j = from; j < to; ++j)
+            (void)mbar_wait_bounded(sig, &full[j % kTmaStages], (uint32_t)(j / kTmaStages) & 1u);
+    };
+
+    // The shard is this rank's own data, ready before any barrier: the first
+    // loads go out before the ARRIVE wait, whose latency they overlap.  Only
+    // the stores into the outputs (peers' buffers) wait for it.
+    int nissued = 0;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kTmaStages; ++i) mbar_init(&full[i], 1);
+        fence_mbar_init();
+        int64_t cs, cd;
+        uint32_t cl;
+        while (nissued < kTmaStages && next(cs, cd, cl)) issue(nissued++, cs, cd, cl);
+    }
+    if (b == 0) emit(sig, RR_BARRIER_ARRIVE, r, 0);
+    else __syncthreads();
+    if (!wait(sig, RR_BARRIER_ARRIVE, r, 0, &s_ok)) {
+        if (threadIdx.x == 0) drain(0, nissued);
+        return;
+    }
+
     if (threadIdx.x >= 32) {
         // Everything the bulk engine does not take.
         const int tid = threadIdx.x - 32, nthr = kTmaThreads - 32;
-        for (int s = sfirst; s < a.nsplit && a.off[s] < x1; ++s) {
+        for (int sp = sfirst; sp < a.nsplit && a.off[sp] < x1; ++sp) {
             int64_t p0, p1, d0, q0, qend, e0;
-            if (!piece_of(a, r, s, x0, x1, p0, p1, d0)) continue;
-            if (bulk_part(a, r, s, x0, x1, q0, qend, e0))
+            if (!piece_of(a, r, sp, x0, x1, p0, p1, d0)) continue;
+            if (bulk_part(a, r, sp, x0, x1, q0, qend, e0))
                 push_bytes(a, src + qend, d0 + (qend - p0), p1 - qend, tid, nthr);
             else
                 push_bytes(a, src + p0, d0, p1 - p0, tid, nthr);
         }
     } else if (threadIdx.x == 0) {
-        // Chunk iterator over the bulk parts of the region's pieces.
-        int s = sfirst - 1;
-        int64_t pos = 0, pend = 0, dpos = 0;
-        auto next = [&](int64_t &cs, int64_t &cd, uint32_t &cl) -> bool {
-            while (pos >= pend) {
-                ++s;
-                if (s >= a.nsplit || a.off[s] >= x1) return false;
-                int64_t p0, pe, d0;
-                if (bulk_part(a, r, s, x0, x1, p0, pe, d0)) {
-                    pos = p0;
-                    pend = pe;
-                    dpos = d0;
-                }
-            }
-            const int64_t left = pend - pos;
-            cl = (uint32_t)(left < kTmaChunk ? left : kTmaChunk);
-            cs = pos;
-            cd = dpos;
-            pos += cl;
-            dpos += cl;
-            return true;
-        };
-        int64_t dst_of[kTmaStages];
-        uint32_t len_of[kTmaStages];
-        auto issue = [&](int k, int64_t cs, int64_t cd, uint32_t cl) {
-            const int st = k % kTmaStages;
-            dst_of[st] = cd;
-            len_of[st] = cl;
-            mbar_expect_tx(&full[st], cl);
-            bulk_load(stage_mem + (size_t)st * kTmaChunk, src + cs, cl, &full[st]);
-        };
-        int nissued = 0;
-        {
-            int64_t cs, cd;
-            uint32_t cl;
-            while (nissued < kTmaStages && next(cs, cd, cl)) issue(nissued++, cs, cd, cl);
-        }
         bool ok = true;
         for (int k = 0; k < nissued; ++k) {
             const int st = k % kTmaStages;
-            if (!mbar_wait_bounded(a.sig, &full[st], (uint32_t)(k / kTmaStages) & 1u)) {
+            if (!mbar_wait_bounded(sig, &full[st], (uint32_t)(k / kTmaStages) & 1u)) {
                 ok = false;
-                // Let the loads already in flight land before this block's
-                // shared memory can be handed to anyone else.
-                for (int j = k; j < nissued; ++j)
-                    (void)mbar_wait_bounded(a.sig, &full[j % kTmaStages], (uint32_t)(j / kTmaStages) & 1u);
+                drain(k, nissued);
                 break;
             }
             fence_async_shared();
@@ -232,10 +246,17 @@ __global__ void __launch_bounds__(kTmaThreads) gather_kernel_tma(const __grid_co
         }
         bulk_wait_all();
         fence_async_global();
-        if (!ok) record_timeout(a.sig, RR_BARRIER_END, r, b);
+        if (!ok) record_timeout(sig, RR_BARRIER_END, r, b);
     }
-    emit(a.sig, RR_BARRIER_END, r, b);
-    wait(a.sig, RR_BARRIER_END, r, b, &s_ok);
+    emit(sig, RR_BARRIER_END, r, b);
+    wait(sig, RR_BARRIER_END, r, b, &s_ok);
+}
+
+__global__ void __launch_bounds__(kTmaThreads) gather_kernel_tma(const __grid_constant__ GatherArgs a)
+{
+    const SignalArgs sig = begin_call(a.sig);
+    gather_kernel_tma_body(a, sig);
+    end_call(sig);
 }
 
 KernelChoice gather_kernel_for(int engine)

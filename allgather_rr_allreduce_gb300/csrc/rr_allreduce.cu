@@ -190,8 +190,7 @@ __device__ __forceinline__ void reduce_share(const ReduceArgs &a, int r, int64_t
 //      the copy, and the staged bytes are read back while still in L2.
 //  END barrier on block b: no rank leaves while a peer still reads its chunk.
 template <class Op, int WMAX, bool kCopy>
-__global__ void __launch_bounds__(kReduceThreads, 2)
-    oneshot_kernel(const __grid_constant__ ReduceArgs a)
+__device__ __forceinline__ void oneshot_kernel_body(const ReduceArgs &a, const SignalArgs &sig)
 {
     __shared__ int s_ok;
     const int r = blockIdx.x / a.B;
@@ -217,10 +216,10 @@ __global__ void __launch_bounds__(kReduceThreads, 2)
                     copy_vectors(static_cast<const uint4 *>(a.in[r]) + s0, static_cast<uint4 *>(a.buf[r]) + s0,
                                  s1 - s0);
                 if (ks == R - 1 && has_tail) copy_tail<Op::kBytes>(a.in[r], a.buf[r], t0, ntail);
-                emit_round(a.sig, 0, r, b, ks);
+                emit_round(sig, 0, r, b, ks);
             }
             if (k < 0) continue;
-            if (!wait_round(a.sig, 0, r, b, k, &s_ok)) return;
+            if (!wait_round(sig, 0, r, b, k, &s_ok)) return;
             const int64_t s0 = v0 + (int64_t)k * P;
             reduce_share<Op, WMAX, true>(a, r, s0, min(v1, s0 + P));
             if (k == R - 1 && has_tail)
@@ -229,8 +228,8 @@ __global__ void __launch_bounds__(kReduceThreads, 2)
                         combine_scalar<Op>(a.buf, a.W, a.out[a.qlist[m]], t0 + e);
         }
     } else {
-        if (b == 0) emit(a.sig, RR_BARRIER_ARRIVE, r, 0);
-        if (!wait(a.sig, RR_BARRIER_ARRIVE, r, 0, &s_ok)) return;
+        if (b == 0) emit(sig, RR_BARRIER_ARRIVE, r, 0);
+        if (!wait(sig, RR_BARRIER_ARRIVE, r, 0, &s_ok)) return;
         reduce_share<Op, WMAX, false>(a, r, v0, v1);
         if (has_tail)
             for (int m = r; m < a.nout; m += a.W)
@@ -238,8 +237,16 @@ __global__ void __launch_bounds__(kReduceThreads, 2)
                     combine_scalar<Op>(a.buf, a.W, a.out[a.qlist[m]], t0 + e);
     }
 
-    emit(a.sig, RR_BARRIER_END, r, b);
-    wait(a.sig, RR_BARRIER_END, r, b, &s_ok);
+    emit(sig, RR_BARRIER_END, r, b);
+    wait(sig, RR_BARRIER_END, r, b, &s_ok);
+}
+
+template <class Op, int WMAX, bool kCopy>
+__global__ void __launch_bounds__(kReduceThreads, 2) oneshot_kernel(const __grid_constant__ ReduceArgs a)
+{
+    const SignalArgs sig = begin_call(a.sig);
+    oneshot_kernel_body<Op, WMAX, kCopy>(a, sig);
+    end_call(sig);
 }
 
 // ------------------------------------------------------------------ two-shot
@@ -261,8 +268,7 @@ __global__ void __launch_bounds__(kReduceThreads, 2)
 //  reduction is issued in between), so the flag latency is hidden and the
 //  reduced chunk is copied out while it is still in L2.  END barrier.
 template <class Op, int WMAX, bool kCopy, bool kPush>
-__global__ void __launch_bounds__(kReduceThreads, 2)
-    twoshot_kernel(const __grid_constant__ ReduceArgs a)
+__device__ __forceinline__ void twoshot_kernel_body(const ReduceArgs &a, const SignalArgs &sig)
 {
     __shared__ int s_ok;
     __shared__ CopyDesc s_desc[RR_MAX_WORLD];
@@ -350,23 +356,23 @@ __global__ void __launch_bounds__(kReduceThreads, 2)
             reduce_vectors_bcast<Op, WMAX, kCopy>(a, s0, s1);
             if (k == R - 1 && has_tail && r == W - 1)
                 for (int e = threadIdx.x; e < ntail; e += kReduceThreads)
-                    for (int q = 0; q < W; ++q) combine_scalar<Op>(a.buf, W, a.out[q], t0 + e);
+                    combine_scalar_to<Op>(a.buf, W, a.out, W, t0 + e);
         };
         if constexpr (kCopy) {
             // iteration k: stage k+1; reduce and broadcast k
             for (int k = -1; k < R; ++k) {
                 if (k + 1 < R) {
                     copy_round(k + 1, true);
-                    emit_round(a.sig, 0, r, b, k + 1);
+                    emit_round(sig, 0, r, b, k + 1);
                 }
                 if (k >= 0) {
-                    if (!wait_round(a.sig, 0, r, b, k, &s_ok)) return;
+                    if (!wait_round(sig, 0, r, b, k, &s_ok)) return;
                     reduce_push(k);
                 }
             }
         } else {
-            if (b == 0) emit(a.sig, RR_BARRIER_ARRIVE, r, 0);
-            if (!wait(a.sig, RR_BARRIER_ARRIVE, r, 0, &s_ok)) return;
+            if (b == 0) emit(sig, RR_BARRIER_ARRIVE, r, 0);
+            if (!wait(sig, RR_BARRIER_ARRIVE, r, 0, &s_ok)) return;
             for (int k = 0; k < R; ++k) reduce_push(k);
         }
     } else if constexpr (kCopy) {
@@ -374,36 +380,44 @@ __global__ void __launch_bounds__(kReduceThreads, 2)
         for (int k = -1; k <= R; ++k) {
             if (k + 1 < R) {
                 copy_round(k + 1, true);
-                emit_round(a.sig, 0, r, b, k + 1);
+                emit_round(sig, 0, r, b, k + 1);
             }
             if (k >= 0 && k < R) {
-                if (!wait_round(a.sig, 0, r, b, k, &s_ok)) return;
+                if (!wait_round(sig, 0, r, b, k, &s_ok)) return;
                 reduce_own(k);
-                emit_round(a.sig, 1, r, b, k);
+                emit_round(sig, 1, r, b, k);
             }
             if (k >= 1) {
-                if (!wait_round(a.sig, 1, r, b, k - 1, &s_ok)) return;
+                if (!wait_round(sig, 1, r, b, k - 1, &s_ok)) return;
                 copy_round(k - 1, false);
             }
         }
     } else {
-        if (b == 0) emit(a.sig, RR_BARRIER_ARRIVE, r, 0);
-        if (!wait(a.sig, RR_BARRIER_ARRIVE, r, 0, &s_ok)) return;
+        if (b == 0) emit(sig, RR_BARRIER_ARRIVE, r, 0);
+        if (!wait(sig, RR_BARRIER_ARRIVE, r, 0, &s_ok)) return;
         // iteration k: reduce k+1; gather k
         for (int k = -1; k < R; ++k) {
             if (k + 1 < R) {
                 reduce_own(k + 1);
-                emit_round(a.sig, 1, r, b, k + 1);
+                emit_round(sig, 1, r, b, k + 1);
             }
             if (k >= 0) {
-                if (!wait_round(a.sig, 1, r, b, k, &s_ok)) return;
+                if (!wait_round(sig, 1, r, b, k, &s_ok)) return;
                 copy_round(k, false);
             }
         }
     }
 
-    emit(a.sig, RR_BARRIER_END, r, b);
-    wait(a.sig, RR_BARRIER_END, r, b, &s_ok);
+    emit(sig, RR_BARRIER_END, r, b);
+    wait(sig, RR_BARRIER_END, r, b, &s_ok);
+}
+
+template <class Op, int WMAX, bool kCopy, bool kPush>
+__global__ void __launch_bounds__(kReduceThreads, 2) twoshot_kernel(const __grid_constant__ ReduceArgs a)
+{
+    const SignalArgs sig = begin_call(a.sig);
+    twoshot_kernel_body<Op, WMAX, kCopy, kPush>(a, sig);
+    end_call(sig);
 }
 
 // ------------------------------------------------------------ one-shot, TMA
@@ -443,8 +457,7 @@ struct TileWalk {
 };
 
 template <class Op, int WMAX>
-__global__ void __launch_bounds__(kRtThreads, 1)
-    oneshot_tma_kernel(const __grid_constant__ ReduceArgs a)
+__device__ __forceinline__ void oneshot_tma_kernel_body(const ReduceArgs &a, const SignalArgs &sig)
 {
     constexpr int S = RtStages<WMAX>::kStages;
     extern __shared__ __align__(128) unsigned char stages[];  // [S][WMAX][kRtTileBytes]
@@ -469,9 +482,9 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         fence_mbar_init();
         s_fail = 0;
     }
-    if (b == 0) emit(a.sig, RR_BARRIER_ARRIVE, r, 0);
+    if (b == 0) emit(sig, RR_BARRIER_ARRIVE, r, 0);
     else __syncthreads();
-    if (!wait(a.sig, RR_BARRIER_ARRIVE, r, 0, &s_ok)) return;
+    if (!wait(sig, RR_BARRIER_ARRIVE, r, 0, &s_ok)) return;
 
     const int64_t L = v1 - v0;
     TileWalk walk{0, 0, L > 0 ? L : 1, v0};
@@ -489,7 +502,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
             bool ok = true;
             while (walk.next(m, v, n)) {
                 const int st = i % S;
-                if (i >= S && !mbar_wait_bounded(a.sig, &empty[st], (uint32_t)((i / S) - 1) & 1u)) {
+                if (i >= S && !mbar_wait_bounded(sig, &empty[st], (uint32_t)((i / S) - 1) & 1u)) {
                     ok = false;
                     break;
                 }
@@ -502,7 +515,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
             if (!ok) {
                 // Let every load already issued land before the block can exit.
                 for (int j = max(0, i - S); j < i; ++j)
-                    (void)mbar_wait_bounded(a.sig, &full[j % S], (uint32_t)(j / S) & 1u);
+                    (void)mbar_wait_bounded(sig, &full[j % S], (uint32_t)(j / S) & 1u);
                 s_fail = 1;
             }
         }
@@ -512,7 +525,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         int i = 0;
         while (walk.next(m, v, n)) {
             const int st = i % S;
-            if (!mbar_wait_bounded(a.sig, &full[st], (uint32_t)(i / S) & 1u)) {
+            if (!mbar_wait_bounded(sig, &full[st], (uint32_t)(i / S) & 1u)) {
                 s_fail = 1;
                 break;
             }
@@ -537,11 +550,19 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     }
     __syncthreads();
     if (s_fail) {
-        if (threadIdx.x == 0) record_timeout(a.sig, RR_BARRIER_END, r, b);
+        if (threadIdx.x == 0) record_timeout(sig, RR_BARRIER_END, r, b);
         return;
     }
-    emit(a.sig, RR_BARRIER_END, r, b);
-    wait(a.sig, RR_BARRIER_END, r, b, &s_ok);
+    emit(sig, RR_BARRIER_END, r, b);
+    wait(sig, RR_BARRIER_END, r, b, &s_ok);
+}
+
+template <class Op, int WMAX>
+__global__ void __launch_bounds__(kRtThreads, 1) oneshot_tma_kernel(const __grid_constant__ ReduceArgs a)
+{
+    const SignalArgs sig = begin_call(a.sig);
+    oneshot_tma_kernel_body<Op, WMAX>(a, sig);
+    end_call(sig);
 }
 
 // ------------------------------------------------- copy_mode, warp-specialised
@@ -554,8 +575,9 @@ __global__ void __launch_bounds__(kRtThreads, 1)
 // as 16 KiB tiles through a ring of shared-memory stages: cp.async.bulk
 // global -> shared completing on a `full` mbarrier, then cp.async.bulk shared
 // -> global in a bulk group.  Loads run kSwAhead tiles ahead of the stores.
-// After each store it waits until at most kSwAhead - 1 bulk groups are
-// incomplete; every round whose tiles have all landed is then published:
+// After each store it lets at most kSwReading bulk groups still read shared
+// memory (stage recycling) and at most kSwLanding still land in global
+// memory; every round whose tiles have all landed is then published:
 // async-proxy fence, round flag k (STAGE) released to every listener.  Only
 // this lane waits for the stores to land.
 // Consumers (the other 8 warps): per round, wait for round flag k of block b
@@ -563,21 +585,28 @@ __global__ void __launch_bounds__(kRtThreads, 1)
 // the staged buffers, which the producers wrote moments ago (L2).
 // The ragged tail is staged by the consumers before the roles split, so the
 // producer's first release covers it.  END barrier over the whole block.
-constexpr int kSwConsumerWarps = 8;
+constexpr int kSwConsumerWarps = 16;
 constexpr int kSwConsumers = 32 * kSwConsumerWarps;
 constexpr int kSwThreads = kSwConsumers + 32;
-constexpr int kSwStages = 8;
-constexpr int kSwAhead = 4;          // loads in flight ahead of the store being issued
+constexpr int kSwStages = 12;
+constexpr int kSwAhead = 6;          // loads in flight ahead of the store being issued
+constexpr int kSwReading = 5;        // store groups allowed to be still reading shared memory
+constexpr int kSwLanding = 16;       // store groups allowed to be still landing in global memory
+constexpr int kSwRoundRing = 32;     // rounds of the last kSwRoundRing tiles are remembered
 constexpr int kSwTileBytes = 16384;
-constexpr int kSwSmem = kSwStages * kSwTileBytes;
-static_assert(kSwAhead < kSwStages, "the ring must hold the loads ahead and the stores in flight");
+constexpr int kSwSmem = kSwStages * kSwTileBytes;  // 192 KiB
+// The stage a new load reuses (tile t + kSwAhead - kSwStages) must have been
+// read by its store (tiles <= t - kSwReading), and the round of the oldest
+// tile not yet known to have landed must still be remembered.
+static_assert(kSwAhead + kSwReading <= kSwStages, "stage reused before its store read it");
+static_assert(kSwLanding + kSwAhead < kSwRoundRing, "round ring too short");
 
 template <class Op, int WMAX, bool kTwoShot>
-__global__ void __launch_bounds__(kSwThreads, 1) staged_kernel(const __grid_constant__ ReduceArgs a)
+__device__ __forceinline__ void staged_kernel_body(const ReduceArgs &a, const SignalArgs &sig)
 {
     extern __shared__ __align__(128) unsigned char stages[];
     __shared__ __align__(8) uint64_t full[kSwStages];
-    __shared__ int tile_round[kSwStages];
+    __shared__ int tile_round[kSwRoundRing];
     __shared__ int64_t tile_off[kSwStages];   // byte offset within the rank buffer
     __shared__ uint32_t tile_len[kSwStages];
     __shared__ int64_t s_c0[RR_MAX_WORLD], s_c1[RR_MAX_WORLD];
@@ -657,7 +686,7 @@ __global__ void __launch_bounds__(kSwThreads, 1) staged_kernel(const __grid_cons
                 uint32_t len;
                 if (!next_tile(kr, off, len)) return false;
                 const int st = t % kSwStages;
-                tile_round[st] = kr;
+                tile_round[t % kSwRoundRing] = kr;
                 tile_off[st] = off;
                 tile_len[st] = len;
                 mbar_expect_tx(&full[st], len);
@@ -669,24 +698,26 @@ __global__ void __launch_bounds__(kSwThreads, 1) staged_kernel(const __grid_cons
             bool ok = true;
             for (int t = 0; t < issued; ++t) {
                 const int st = t % kSwStages;
-                if (!mbar_wait_bounded(a.sig, &full[st], (uint32_t)(t / kSwStages) & 1u)) {
+                if (!mbar_wait_bounded(sig, &full[st], (uint32_t)(t / kSwStages) & 1u)) {
                     ok = false;
                     for (int u = t; u < issued; ++u)
-                        (void)mbar_wait_bounded(a.sig, &full[u % kSwStages], (uint32_t)(u / kSwStages) & 1u);
+                        (void)mbar_wait_bounded(sig, &full[u % kSwStages], (uint32_t)(u / kSwStages) & 1u);
                     break;
                 }
                 fence_async_shared();
                 bulk_store(dst + tile_off[st], stages + (size_t)st * kSwTileBytes, tile_len[st]);
                 bulk_commit();
-                // tiles <= t - (kSwAhead - 1) have landed (their stages are free too)
-                bulk_wait_pending<kSwAhead - 1>();
-                const int done = t - (kSwAhead - 1);
+                // Stage recycling needs only the reads (tiles <= t - kSwReading);
+                // publishing needs the writes landed (tiles <= t - kSwLanding).
+                bulk_wait_read_pending<kSwReading>();
+                bulk_wait_pending<kSwLanding>();
+                const int done = t - kSwLanding;
                 if (done >= 0) {
                     // rounds before the round of tile done+1 are complete
-                    const int upto = (done + 1 < issued) ? tile_round[(done + 1) % kSwStages] : -1;
+                    const int upto = (done + 1 < issued) ? tile_round[(done + 1) % kSwRoundRing] : -1;
                     if (upto > published) {
                         fence_async_global();
-                        for (; published < upto; ++published) emit_round_single(a.sig, 0, r, b, published);
+                        for (; published < upto; ++published) emit_round_single(sig, 0, r, b, published);
                     }
                 }
                 if (issue(issued)) ++issued;
@@ -694,16 +725,16 @@ __global__ void __launch_bounds__(kSwThreads, 1) staged_kernel(const __grid_cons
             bulk_wait_all();
             if (ok) {
                 fence_async_global();
-                for (; published < R; ++published) emit_round_single(a.sig, 0, r, b, published);
+                for (; published < R; ++published) emit_round_single(sig, 0, r, b, published);
             } else {
                 s_fail = 1;
-                record_timeout(a.sig, RR_BARRIER_STAGE, r, b);
+                record_timeout(sig, RR_BARRIER_STAGE, r, b);
             }
         }
     } else {
         const GroupSync sync{kSwConsumers};
         for (int k = 0; k < R; ++k) {
-            if (!wait_round(a.sig, 0, r, b, k, &s_ok, sync)) {
+            if (!wait_round(sig, 0, r, b, k, &s_ok, sync)) {
                 if (threadIdx.x == 0) s_fail = 1;
                 break;
             }
@@ -714,7 +745,7 @@ __global__ void __launch_bounds__(kSwThreads, 1) staged_kernel(const __grid_cons
                 reduce_vectors_bcast<Op, WMAX, true, kSwConsumers>(a, rs, re);
                 if (k == R - 1 && has_tail && r == W - 1)
                     for (int e = threadIdx.x; e < ntail; e += kSwConsumers)
-                        for (int q = 0; q < W; ++q) combine_scalar<Op>(a.buf, W, a.out[q], t0 + e);
+                        combine_scalar_to<Op>(a.buf, W, a.out, W, t0 + e);
             } else {
                 const int64_t c1 = s_c1[0];
                 const int64_t rs = min(c1, s_c0[0] + (int64_t)k * P);
@@ -729,8 +760,16 @@ __global__ void __launch_bounds__(kSwThreads, 1) staged_kernel(const __grid_cons
     }
     __syncthreads();
     if (s_fail) return;
-    emit(a.sig, RR_BARRIER_END, r, b);
-    wait(a.sig, RR_BARRIER_END, r, b, &s_ok);
+    emit(sig, RR_BARRIER_END, r, b);
+    wait(sig, RR_BARRIER_END, r, b, &s_ok);
+}
+
+template <class Op, int WMAX, bool kTwoShot>
+__global__ void __launch_bounds__(kSwThreads, 1) staged_kernel(const __grid_constant__ ReduceArgs a)
+{
+    const SignalArgs sig = begin_call(a.sig);
+    staged_kernel_body<Op, WMAX, kTwoShot>(a, sig);
+    end_call(sig);
 }
 
 // ------------------------------------------------------------------ dispatch

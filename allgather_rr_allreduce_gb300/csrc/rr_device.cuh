@@ -240,6 +240,12 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // At most N bulk groups still incomplete (the older ones' writes have landed).
 template <int N>
 __device__ __forceinline__ void bulk_wait_pending() { asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory"); }
+// At most N bulk groups still reading their shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read_pending()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
 __device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
@@ -257,6 +263,47 @@ __device__ __forceinline__ bool mbar_wait_bounded(const SignalArgs &s, uint64_t 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// ------------------------------------------------------------ call entry / exit
+// Generation of this call.  Host counter: as passed.  Device counter: every
+// block reads the value the previous call on the pad left (the kernel
+// boundary orders that write before this launch) and uses the next one.
+__device__ __forceinline__ uint64_t next_generation(uint64_t g64)
+{
+    g64 += 1;
+    if ((uint32_t)g64 == 0) g64 += 2;  // g is never 0; the parity is kept
+    return g64;
+}
+
+__device__ __forceinline__ SignalArgs begin_call(const SignalArgs &in)
+{
+    SignalArgs s = in;
+    if (s.dev_gen) {
+        const uint64_t g64 = next_generation(*(volatile uint64_t *)s.dev_gen);
+        s.g = (uint32_t)g64;
+        s.rbase = g64 << kRoundBits;
+    }
+    return s;
+}
+
+// Every block passes here once, whatever path it took.  With the device
+// counter, the last block to arrive (all others have finished, so all have
+// read the counter) resets the tally and stores this call's generation for
+// the next call.
+__device__ __forceinline__ void end_call(const SignalArgs &s)
+{
+    if (!s.dev_gen) return;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const uint32_t total = gridDim.x * gridDim.y * gridDim.z;
+        if (atomicAdd(s.done, 1u) == total - 1u) {
+            *(volatile uint32_t *)s.done = 0u;
+            *(volatile uint64_t *)s.dev_gen = s.rbase >> kRoundBits;
+            __threadfence();
+        }
+    }
 }
 
 // ---------------------------------------------------------------- arithmetic
@@ -356,7 +403,33 @@ __device__ __forceinline__ uint4 combine(const uint4 (&x)[WMAX], int W)
 }
 
 // Element e of the ragged tail (fewer than kEPV elements after the last whole
-// vector): the same rule as combine(), one element at a time.
+// vector): the same rule as combine(), one element at a time, stored into
+// outputs dst[0..ndst) after all W loads (so an output may be a rank buffer).
+template <class Op>
+__device__ __forceinline__ void combine_scalar_to(void *const *bufs, int W, void *const *dst, int ndst, int64_t e)
+{
+    uint32_t res;
+    if constexpr (Op::kBytes == 2) {
+        float acc = Op::widen(__ldcg(reinterpret_cast<const unsigned short *>(bufs[0]) + e));
+        for (int r = 1; r < W; ++r)
+            acc = __fadd_rn(acc, Op::widen(__ldcg(reinterpret_cast<const unsigned short *>(bufs[r]) + e)));
+        res = Op::narrow(acc);
+        for (int q = 0; q < ndst; ++q) reinterpret_cast<unsigned short *>(dst[q])[e] = (unsigned short)res;
+    } else {
+        auto ld = [&](int r) -> uint32_t { return __ldcg(reinterpret_cast<const unsigned int *>(bufs[r]) + e); };
+        if constexpr (Op::kKind == kF32) {
+            float acc = __uint_as_float(ld(0));
+            for (int r = 1; r < W; ++r) acc = __fadd_rn(acc, __uint_as_float(ld(r)));
+            res = __float_as_uint(acc);
+        } else {
+            uint32_t acc = ld(0);
+            for (int r = 1; r < W; ++r) acc += ld(r);
+            res = acc;
+        }
+        for (int q = 0; q < ndst; ++q) reinterpret_cast<unsigned int *>(dst[q])[e] = res;
+    }
+}
+
 template <class Op>
 __device__ __forceinline__ void combine_scalar(void *const *bufs, int W, void *dst, int64_t e)
 {

@@ -44,6 +44,12 @@ struct SignalArgs {
     int W;
     int Bmax;
     int inject;          // -1, or rank*4 + barrier whose flags are never emitted
+    // Device-resident generation (graph-capturable calls): when non-null, g
+    // and rbase are not taken from this struct but from *dev_gen, the 64-bit
+    // counter the previous call left; the last block of the call to finish
+    // (counted in *done) advances it.
+    uint64_t *dev_gen;
+    uint32_t *done;
 };
 
 // One-shot and two-shot allreduce.

@@ -293,7 +293,48 @@ def latency_sweep(rr, stream, reps=1000, batch=250):
                 out["issue_bound_oneshot"][str(nbytes)] = round(1000.0 * e0.elapsed_time(e1) / reps, 3)
     pad.status(stream)
     pad.close()
+    out.update(graph_latency(rr, stream, batch=batch))
     return out
+
+
+def graph_latency(rr, stream, batch=250, reps=3):
+    """The same calls captured in a CUDA graph (pad with the device-resident
+    generation counter), replayed back to back: GPU time per call."""
+    res = {"graph_oneshot": {}, "graph_twoshot": {}}
+    pad = rr.rr_signal_pad_create(W)
+    pad.set_option("device_generation", 1)
+    g = torch.Generator(device="cuda").manual_seed(workloads.LATENCY["seed_base"] + 1)
+    for nbytes in workloads.LATENCY["bytes_per_rank"]:
+        n = nbytes // EB
+        x = (torch.rand((W, n), generator=g, device="cuda") * 2 - 1).to(torch.bfloat16)
+        y = torch.empty((W, n), dtype=torch.bfloat16, device="cuda")
+        rows_x = [x[r].data_ptr() for r in range(W)]
+        rows_y = [y[r].data_ptr() for r in range(W)]
+        for algo in ("oneshot", "twoshot"):
+            fn = getattr(rr, f"rr_allreduce_{algo}")
+            with torch.cuda.stream(stream):
+                fn(None, rows_x, rows_y, W, n, "bf16", 0, pad, stream)
+            stream.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                cs = torch.cuda.current_stream()
+                for _ in range(batch):
+                    fn(None, rows_x, rows_y, W, n, "bf16", 0, pad, cs)
+            graph.replay()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(reps):
+                    graph.replay()
+                e1.record(stream)
+            e1.synchronize()
+            res[f"graph_{algo}"][str(nbytes)] = round(1000.0 * e0.elapsed_time(e1) / (reps * batch), 3)
+            del graph
+    pad.status(stream)
+    pad.close()
+    return res
 
 
 def fsdp_28_layers(rr, stream):

@@ -84,7 +84,8 @@ typedef enum {
     RR_OPT_ROUND_BYTES = 4,     /* bytes per rank per round of a pipelined chunk (copy_mode
                                    staging, two-shot); 0 = automatic (64 KiB one-shot,
                                    32 KiB two-shot) */
-    RR_OPT_REDUCE_ENGINE = 5,   /* 0 = automatic, 1 = 128-bit loads/stores, 2 = bulk-copy (TMA)
+    RR_OPT_REDUCE_ENGINE = 5,   /* 0 = automatic (bulk copies for copy_mode, loads/stores
+                                   otherwise), 1 = 128-bit loads/stores, 2 = bulk-copy (TMA)
                                    engine: copy_mode off, the one-shot's loads stream into a
                                    shared-memory ring; copy_mode on, a producer warp stages the
                                    inputs by bulk copies while the other warps reduce (the
@@ -93,8 +94,14 @@ typedef enum {
                                    copies the other owners' reduced chunks after the MID
                                    barrier), 2 = push (each owner stores its reduced chunk into
                                    every output; no MID barrier) */
+    RR_OPT_DEVICE_GENERATION = 7, /* 0 = each call takes its generation from a host counter
+                                   (default); 1 = from a counter in device memory that the
+                                   last block of each call advances, so that calls captured
+                                   in a CUDA graph stay correct on every replay.  Switching
+                                   synchronises the device; the pad must be idle */
     /* read-only */
-    RR_OPT_GENERATION = 16,     /* generation flag value of the last call */
+    RR_OPT_GENERATION = 16,     /* generation flag value of the last call (device-generation
+                                   mode: reads the device counter, synchronising the device) */
     RR_OPT_LAST_GRID = 17,      /* blocks launched by the last call */
     RR_OPT_LAST_BLOCKS_PER_RANK = 18,
     RR_OPT_LAST_ENGINE = 19,    /* engine the last call used (1 = loads/stores, 2 = bulk copies) */
@@ -198,9 +205,20 @@ rr_status rr_allreduce_oneshot(const void *const *inputs, void *const *rank_bufs
  * up to whole 256-byte granules), the last segment short or empty, and the
  * elements after the last whole vector are owned by rank W-1.
  *
- * Arguments as rr_allreduce_oneshot, except that every outputs[r] is required
- * (peers read the reduced segments from it).  Barriers: ARRIVE or STAGE,
- * MID between the phases, END.  Results are bit-identical to the one-shot.
+ * Arguments as rr_allreduce_oneshot, except that every outputs[r] is required.
+ * Two allgather modes (RR_OPT_TWOSHOT_MODE): push (default), where each owner
+ * stores its reduced chunk into every output, as the owner-side multicast
+ * store of the Triton kernel does; pull, where each rank copies the other
+ * owners' reduced chunks out of their outputs after the MID barrier.
+ * Barriers: ARRIVE or STAGE, MID (pull only), END.  Results are bit-identical
+ * to the one-shot.
+ *
+ * In place: with copy_mode off, outputs[r] may equal rank_bufs[r] (exactly,
+ * for any subset of r); the sum then replaces the rank buffers, as the Triton
+ * kernel's in-place allreduce does.  (Every chunk is read from all buffers
+ * and written by the same block; in pull mode the MID barrier orders every
+ * owner's reads before the overwrite.)  The one-shot never runs in place: a
+ * peer may still be reading the buffer being overwritten.
  */
 rr_status rr_allreduce_twoshot(const void *const *inputs, void *const *rank_bufs,
                                void *const *outputs, int world_size, int64_t numel,

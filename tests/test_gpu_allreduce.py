@@ -110,7 +110,7 @@ def test_oneshot_subset_of_outputs(rr, materialise, copy_mode):
     outs.check_guards()
 
 
-@pytest.mark.parametrize("blocks", [1, 2, 7, 64])
+@pytest.mark.parametrize("blocks", [1, 2, 7, 32])
 @pytest.mark.parametrize("algo", ["oneshot", "twoshot", "twoshot_pull"])
 def test_fixed_blocks_per_rank(rr, blocks, algo):
     """The result does not depend on how many blocks each rank runs,
@@ -257,6 +257,63 @@ def test_staged_rounds_and_blocks(rr, round_bytes, blocks, algo):
         pad.set_option("round_bytes", 0)
     for r in range(W):
         assert_bitwise(outs.host(r), want, f"{algo} round_bytes={round_bytes} blocks={blocks} output {r}")
+
+
+@pytest.mark.parametrize("mode", ["twoshot", "twoshot_pull"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32", "int32"])
+@pytest.mark.parametrize("W,N", [(2, 4099), (3, 12345), (8, (1 << 20) + 3), (16, 10000), (5, 7)])
+def test_twoshot_in_place(rr, mode, dtype, W, N):
+    """outputs[r] == rank_bufs[r]: the sum replaces every rank buffer."""
+    ins = workloads.rank_buffers(W, N, dtype, dist_for(dtype), seed_base=1100 * W + N % 71)
+    want = oracle.allreduce(ins, dtype)
+    pad = pad_for(rr, W)
+    bufs = RankBuffers(W, N, dtype)
+    bufs.fill(ins)
+    pad.set_option("twoshot_mode", 1 if mode == "twoshot_pull" else 2)
+    try:
+        rr.rr_allreduce_twoshot(None, bufs.ptrs, bufs.ptrs, W, N, dtype, 0, pad)
+        pad.status()
+    finally:
+        pad.set_option("twoshot_mode", 0)
+    for r in range(W):
+        assert_bitwise(bufs.host(r), want, f"{mode} in place, rank {r}")
+
+
+def test_in_place_refused_where_it_would_race(rr):
+    W, N = 4, 4096
+    pad = pad_for(rr, W)
+    bufs = RankBuffers(W, N, "bf16")
+    src = RankBuffers(W, N, "bf16")
+    with pytest.raises(rr.RRError) as e:
+        rr.rr_allreduce_oneshot(None, bufs.ptrs, bufs.ptrs, W, N, "bf16", 0, pad)
+    assert e.value.status == rr.RR_ERR_ALIAS
+    with pytest.raises(rr.RRError) as e:
+        rr.rr_allreduce_twoshot(src.ptrs, bufs.ptrs, bufs.ptrs, W, N, "bf16", 1, pad)
+    assert e.value.status == rr.RR_ERR_ALIAS
+    with pytest.raises(rr.RRError) as e:  # a partial overlap is never in place
+        rr.rr_allreduce_twoshot(None, bufs.ptrs, [p + 16 for p in bufs.ptrs], W, N - 8, "bf16", 0, pad)
+    assert e.value.status == rr.RR_ERR_ALIAS
+    pad.status()
+
+
+@pytest.mark.parametrize("algo", ["oneshot", "twoshot", "twoshot_pull"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32", "int32"])
+@pytest.mark.parametrize("W,N", SHAPES, ids=[f"W{w}_N{n}" for w, n in SHAPES])
+def test_ldst_copy_mode_matches_oracle(rr, algo, dtype, W, N):
+    """copy_mode on the load/store kernels (staging by every thread, rounds)."""
+    ins = workloads.rank_buffers(W, N, dtype, dist_for(dtype), seed_base=1300 * W + N % 61)
+    want = oracle.allreduce(ins, dtype)
+    pad = pad_for(rr, W)
+    pad.set_option("reduce_engine", 1)
+    try:
+        bufs, src, outs = run_allreduce(rr, algo, W, N, dtype, 1, ins)
+        assert pad.get_option("last_engine") == 1
+    finally:
+        pad.set_option("reduce_engine", 0)
+    for r in range(W):
+        assert_bitwise(outs.host(r), want, f"ldst {algo} output {r}")
+        assert_bitwise(bufs.host(r), ins[r])
+    outs.check_guards()
 
 
 def test_separate_allocations(rr):
