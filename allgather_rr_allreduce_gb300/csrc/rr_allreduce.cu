@@ -31,7 +31,7 @@ struct Unroll {
 
 // dst[v] = combine over r of buf[r][v], for v in [v0, v1).  Thread t takes
 // vectors v0 + t, v0 + t + 256, ...: each warp load is 512 contiguous bytes.
-template <class Op, int WMAX, bool kFromL2, int kThreads = kReduceThreads>
+template <class Op, int WMAX, bool kFromL2, int kThreads = kReduceThreads, bool kStaged = false>
 __device__ __forceinline__ void reduce_vectors(const ReduceArgs &a, void *dst_base, int64_t v0,
                                                int64_t v1)
 {
@@ -46,13 +46,19 @@ __device__ __forceinline__ void reduce_vectors(const ReduceArgs &a, void *dst_ba
             if (v < v1) {
 #pragma unroll
                 for (int r = 0; r < WMAX; ++r)
-                    if (r < W) x[u][r] = ld_vec(static_cast<const uint4 *>(a.buf[r]) + v);
+                    if (r < W) {
+                        if constexpr (kStaged) x[u][r] = ld_vec_stream(static_cast<const uint4 *>(a.buf[r]) + v);
+                        else x[u][r] = ld_vec(static_cast<const uint4 *>(a.buf[r]) + v);
+                    }
             }
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t v = base + (int64_t)u * kThreads;
-            if (v < v1) st_vec(dst + v, combine<Op, WMAX>(x[u], W));
+            if (v < v1) {
+                if constexpr (kStaged) st_vec_stream(dst + v, combine<Op, WMAX>(x[u], W));
+                else st_vec(dst + v, combine<Op, WMAX>(x[u], W));
+            }
         }
     }
 }
@@ -60,7 +66,7 @@ __device__ __forceinline__ void reduce_vectors(const ReduceArgs &a, void *dst_ba
 // Reduce vectors [v0, v1) of the W rank buffers once and store the sum into
 // every output (the two-shot's allgather done as a broadcast by the owner of
 // the chunk, as the owner-side multicast store of the Triton kernel does).
-template <class Op, int WMAX, bool kFromL2, int kThreads = kReduceThreads>
+template <class Op, int WMAX, bool kFromL2, int kThreads = kReduceThreads, bool kStaged = false>
 __device__ __forceinline__ void reduce_vectors_bcast(const ReduceArgs &a, int64_t v0, int64_t v1)
 {
     constexpr int U = Unroll<WMAX, kFromL2>::U;
@@ -73,7 +79,10 @@ __device__ __forceinline__ void reduce_vectors_bcast(const ReduceArgs &a, int64_
             if (v < v1) {
 #pragma unroll
                 for (int r = 0; r < WMAX; ++r)
-                    if (r < W) x[u][r] = ld_vec(static_cast<const uint4 *>(a.buf[r]) + v);
+                    if (r < W) {
+                        if constexpr (kStaged) x[u][r] = ld_vec_stream(static_cast<const uint4 *>(a.buf[r]) + v);
+                        else x[u][r] = ld_vec(static_cast<const uint4 *>(a.buf[r]) + v);
+                    }
             }
         }
 #pragma unroll
@@ -83,7 +92,10 @@ __device__ __forceinline__ void reduce_vectors_bcast(const ReduceArgs &a, int64_
                 const uint4 y = combine<Op, WMAX>(x[u], W);
 #pragma unroll
                 for (int q = 0; q < WMAX; ++q)
-                    if (q < W) st_vec(static_cast<uint4 *>(a.out[q]) + v, y);
+                    if (q < W) {
+                        if constexpr (kStaged) st_vec_stream(static_cast<uint4 *>(a.out[q]) + v, y);
+                        else st_vec(static_cast<uint4 *>(a.out[q]) + v, y);
+                    }
             }
         }
     }
@@ -160,7 +172,7 @@ __device__ __forceinline__ void copy_tail(const void *src, void *dst, int64_t e0
 // ranks whose output is not kept lend their bandwidth.  Every block of index
 // b has passed the same barrier on these vectors, so what each may read is
 // the same.
-template <class Op, int WMAX, bool kFromL2, int kThreads = kReduceThreads>
+template <class Op, int WMAX, bool kFromL2, int kThreads = kReduceThreads, bool kStaged = false>
 __device__ __forceinline__ void reduce_share(const ReduceArgs &a, int r, int64_t s0, int64_t s1)
 {
     const int64_t L = s1 - s0;
@@ -172,7 +184,8 @@ __device__ __forceinline__ void reduce_share(const ReduceArgs &a, int r, int64_t
         const int m = (int)(pos / L);
         const int64_t end = min(hi, (int64_t)(m + 1) * L);
         const int64_t off = pos - (int64_t)m * L;
-        reduce_vectors<Op, WMAX, kFromL2, kThreads>(a, a.out[a.qlist[m]], s0 + off, s0 + off + (end - pos));
+        reduce_vectors<Op, WMAX, kFromL2, kThreads, kStaged>(a, a.out[a.qlist[m]], s0 + off,
+                                                                  s0 + off + (end - pos));
         pos = end;
     }
 }
@@ -679,6 +692,10 @@ __device__ __forceinline__ void staged_kernel_body(const ReduceArgs &a, const Si
             };
             const char *src = static_cast<const char *>(a.in[r]);
             char *dst = static_cast<char *>(a.buf[r]);
+            // Inputs are read once (evict first); staged bytes are read back
+            // by the consumers of every rank within about a round (evict last).
+            const uint64_t read_once = l2_policy_evict_first();
+            const uint64_t keep = l2_policy_evict_last();
             int issued = 0;
             auto issue = [&](int t) -> bool {
                 int kr;
@@ -690,7 +707,7 @@ __device__ __forceinline__ void staged_kernel_body(const ReduceArgs &a, const Si
                 tile_off[st] = off;
                 tile_len[st] = len;
                 mbar_expect_tx(&full[st], len);
-                bulk_load(stages + (size_t)st * kSwTileBytes, src + off, len, &full[st]);
+                bulk_load_hint(stages + (size_t)st * kSwTileBytes, src + off, len, &full[st], read_once);
                 return true;
             };
             while (issued < kSwAhead && issue(issued)) ++issued;
@@ -705,7 +722,7 @@ __device__ __forceinline__ void staged_kernel_body(const ReduceArgs &a, const Si
                     break;
                 }
                 fence_async_shared();
-                bulk_store(dst + tile_off[st], stages + (size_t)st * kSwTileBytes, tile_len[st]);
+                bulk_store_hint(dst + tile_off[st], stages + (size_t)st * kSwTileBytes, tile_len[st], keep);
                 bulk_commit();
                 // Stage recycling needs only the reads (tiles <= t - kSwReading);
                 // publishing needs the writes landed (tiles <= t - kSwLanding).
@@ -742,7 +759,7 @@ __device__ __forceinline__ void staged_kernel_body(const ReduceArgs &a, const Si
                 const int64_t c1 = s_c1[r];
                 const int64_t rs = min(c1, s_c0[r] + (int64_t)k * P);
                 const int64_t re = min(c1, rs + P);
-                reduce_vectors_bcast<Op, WMAX, true, kSwConsumers>(a, rs, re);
+                reduce_vectors_bcast<Op, WMAX, true, kSwConsumers, true>(a, rs, re);
                 if (k == R - 1 && has_tail && r == W - 1)
                     for (int e = threadIdx.x; e < ntail; e += kSwConsumers)
                         combine_scalar_to<Op>(a.buf, W, a.out, W, t0 + e);
@@ -750,7 +767,7 @@ __device__ __forceinline__ void staged_kernel_body(const ReduceArgs &a, const Si
                 const int64_t c1 = s_c1[0];
                 const int64_t rs = min(c1, s_c0[0] + (int64_t)k * P);
                 const int64_t re = min(c1, rs + P);
-                reduce_share<Op, WMAX, true, kSwConsumers>(a, r, rs, re);
+                reduce_share<Op, WMAX, true, kSwConsumers, true>(a, r, rs, re);
                 if (k == R - 1 && has_tail)
                     for (int m = r; m < a.nout; m += W)
                         for (int e = threadIdx.x; e < ntail; e += kSwConsumers)

@@ -15,6 +15,10 @@ namespace rr {
 // coherent across SMs.
 __device__ __forceinline__ uint4 ld_vec(const void *p) { return __ldcg(reinterpret_cast<const uint4 *>(p)); }
 __device__ __forceinline__ void st_vec(void *p, uint4 v) { __stcg(reinterpret_cast<uint4 *>(p), v); }
+// Streaming accesses (evict first): outputs nothing in the call reads back,
+// and staged bytes read for the last time.
+__device__ __forceinline__ void st_vec_stream(void *p, uint4 v) { __stcs(reinterpret_cast<uint4 *>(p), v); }
+__device__ __forceinline__ uint4 ld_vec_stream(const void *p) { return __ldcs(reinterpret_cast<const uint4 *>(p)); }
 
 // ---------------------------------------------------------------- flags
 // Generation flags follow multi_gpu_barrier / block_barrier in "Question and
@@ -232,6 +236,35 @@ __device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_
 {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
                  "r"(bytes)
+                 : "memory");
+}
+// L2 eviction policies for bulk copies: data read once (evict first) and
+// data written to be read back soon by other blocks (evict last).
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void bulk_load_hint(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar,
+                                               uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(sdst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_store_hint(void *gdst, const void *ssrc, uint32_t bytes, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(gdst),
+                 "r"(smem_u32(ssrc)), "r"(bytes), "l"(policy)
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
