@@ -65,6 +65,7 @@ def lib():
             "rr_allreduce_twoshot": [_PP, _PP, _PP, i32, i64, i32, i32, _vp, _vp],
             "rr_allgather": [_PP, _PP, i32, i64, i32, _vp, _vp],
             "rr_allgather_param_contiguous": [_PP, _PP, i32, ctypes.POINTER(i64), i32, i32, _vp, _vp],
+            "rr_allgather_list": [_PP, _PP, i32, i64, i32, _vp, _vp],
         }
         for name, args in sig.items():
             f = getattr(l, name)
@@ -211,6 +212,17 @@ def rr_allgather_param_contiguous(rank_bufs, outputs, world_size, split_sizes, d
     _check(lib().rr_allgather_param_contiguous(pointer_array(rank_bufs), pointer_array(outputs),
                                                world_size, sp, n, dtype_code(dtype),
                                                _pad_handle(pad), stream_handle(stream)))
+
+
+def rr_allgather_list(rank_bufs, output_lists, world_size, numel_per_rank, dtype, pad, stream=None):
+    """output_lists: W entries, each a list of W device buffers (rank q's
+    all_gather tensor_list) or None (not materialised)."""
+    flat = []
+    for row in output_lists:
+        flat.extend([None] * world_size if row is None else list(row))
+    _check(lib().rr_allgather_list(pointer_array(rank_bufs), pointer_array(flat), world_size,
+                                   numel_per_rank, dtype_code(dtype), _pad_handle(pad),
+                                   stream_handle(stream)))
 
 
 def bound_call(name, *args):

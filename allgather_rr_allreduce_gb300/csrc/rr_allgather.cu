@@ -14,6 +14,11 @@
 // Barriers: ARRIVE (every rank has entered, so its output may be written),
 // END on block b (every push of region b has landed before anyone leaves).
 //
+// The list-output gather (torch.distributed.all_gather: output q is W
+// separate buffers) runs the same kernels with a one-split shard whose
+// destination is buffer (q, r) at the shard's own byte offset: only the
+// address of a slot differs (slot_dst in rr_internal.h).
+//
 // Two engines:
 //   ldst: 256 threads move 16-byte vectors (8-byte / 4-byte / 2-byte words
 //         when a piece is not 16-byte aligned).
@@ -44,17 +49,14 @@ __device__ __forceinline__ int first_split_after(const GatherArgs &a, int64_t x)
     return lo;
 }
 
-// Piece of split s inside region [x0, x1) of rank r's shard: shard bytes
-// [p0, p1) and their destination byte offset d0 in every output.
-__device__ __forceinline__ bool piece_of(const GatherArgs &a, int r, int s, int64_t x0, int64_t x1,
-                                         int64_t &p0, int64_t &p1, int64_t &d0)
+// Piece of split s inside region [x0, x1) of a shard: shard bytes [p0, p1).
+__device__ __forceinline__ bool piece_of(const GatherArgs &a, int s, int64_t x0, int64_t x1,
+                                         int64_t &p0, int64_t &p1)
 {
     const int64_t o = a.off[s], e = a.off[s + 1];
     p0 = o > x0 ? o : x0;
     p1 = e < x1 ? e : x1;
-    if (p0 >= p1) return false;
-    d0 = o * a.W + (int64_t)r * (e - o) + (p0 - o);
-    return true;
+    return p0 < p1;
 }
 
 template <class T>
@@ -62,22 +64,22 @@ __device__ __forceinline__ T ld_stream(const T *p) { return __ldcs(p); }
 template <class T>
 __device__ __forceinline__ void st_stream(T *p, T v) { __stcs(p, v); }
 
-// Copy n words of type T from src to every materialised output at byte
-// offset doff, using threads [tid0, tid0 + nthr) of the block.
-template <class T, int U>
-__device__ __forceinline__ void push_words(const GatherArgs &a, const char *src, int64_t doff,
+// Copy n words of type T, rank r's shard bytes from p0 on (split s), to
+// every materialised output, using threads [tid, tid + nthr) of the block.
+template <class T, int U, class Args>
+__device__ __forceinline__ void push_words(const Args &a, int r, int s, const char *src, int64_t p0,
                                            int64_t n, int tid, int nthr)
 {
-    const T *s = reinterpret_cast<const T *>(src);
+    const T *sp = reinterpret_cast<const T *>(src + p0);
     for (int64_t base = tid; base < n; base += (int64_t)nthr * U) {
         T x[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t i = base + (int64_t)u * nthr;
-            if (i < n) x[u] = ld_stream(s + i);
+            if (i < n) x[u] = ld_stream(sp + i);
         }
         for (int q = 0; q < a.nout; ++q) {
-            T *d = reinterpret_cast<T *>(static_cast<char *>(a.out[a.qlist[q]]) + doff);
+            T *d = reinterpret_cast<T *>(slot_dst(a, q, r, s, p0));
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t i = base + (int64_t)u * nthr;
@@ -87,21 +89,24 @@ __device__ __forceinline__ void push_words(const GatherArgs &a, const char *src,
     }
 }
 
-// Copy len bytes (a whole number of elements) with the widest word both
-// sides' alignment allows.  Output bases are 16-byte aligned (checked on the
-// host), so only the offsets and the length decide.
-__device__ __forceinline__ void push_bytes(const GatherArgs &a, const char *src, int64_t doff,
+// Copy shard bytes [p0, p0 + len) (a whole number of elements) with the
+// widest word both sides' alignment allows.  Output bases are 16-byte aligned
+// (checked on the host), so only the offsets and the length decide.
+template <class Args>
+__device__ __forceinline__ void push_bytes(const Args &a, int r, int s, const char *src, int64_t p0,
                                            int64_t len, int tid, int nthr)
 {
-    const uint64_t mis = (uint64_t)(uintptr_t)src | (uint64_t)doff | (uint64_t)len;
-    if ((mis & 15) == 0) push_words<uint4, 4>(a, src, doff, len >> 4, tid, nthr);
-    else if ((mis & 7) == 0) push_words<uint2, 4>(a, src, doff, len >> 3, tid, nthr);
-    else if ((mis & 3) == 0) push_words<unsigned int, 4>(a, src, doff, len >> 2, tid, nthr);
-    else push_words<unsigned short, 4>(a, src, doff, len >> 1, tid, nthr);
+    const uint64_t mis = (uint64_t)(uintptr_t)(src + p0) | (uint64_t)slot_offset(a, r, s, p0) |
+                         (uint64_t)len;
+    if ((mis & 15) == 0) push_words<uint4, 4>(a, r, s, src, p0, len >> 4, tid, nthr);
+    else if ((mis & 7) == 0) push_words<uint2, 4>(a, r, s, src, p0, len >> 3, tid, nthr);
+    else if ((mis & 3) == 0) push_words<unsigned int, 4>(a, r, s, src, p0, len >> 2, tid, nthr);
+    else push_words<unsigned short, 4>(a, r, s, src, p0, len >> 1, tid, nthr);
 }
 
 // ------------------------------------------------------------------ ldst engine
-__device__ __forceinline__ void gather_kernel_ldst_body(const GatherArgs &a, const SignalArgs &sig)
+template <class Args>
+__device__ __forceinline__ void gather_kernel_ldst_body(const Args &a, const SignalArgs &sig)
 {
     __shared__ int s_ok;
     const int r = blockIdx.x / a.B;
@@ -114,16 +119,17 @@ __device__ __forceinline__ void gather_kernel_ldst_body(const GatherArgs &a, con
     const char *src = static_cast<const char *>(a.src[r]);
     if (x0 < x1) {
         for (int s = first_split_after(a, x0); s < a.nsplit && a.off[s] < x1; ++s) {
-            int64_t p0, p1, d0;
-            if (piece_of(a, r, s, x0, x1, p0, p1, d0))
-                push_bytes(a, src + p0, d0, p1 - p0, threadIdx.x, kLdstThreads);
+            int64_t p0, p1;
+            if (piece_of(a, s, x0, x1, p0, p1))
+                push_bytes(a, r, s, src, p0, p1 - p0, threadIdx.x, kLdstThreads);
         }
     }
     emit(sig, RR_BARRIER_END, r, b);
     wait(sig, RR_BARRIER_END, r, b, &s_ok);
 }
 
-__global__ void __launch_bounds__(kLdstThreads) gather_kernel_ldst(const __grid_constant__ GatherArgs a)
+template <class Args>
+__global__ void __launch_bounds__(kLdstThreads) gather_kernel_ldst(const __grid_constant__ Args a)
 {
     const SignalArgs sig = begin_call(a.sig);
     gather_kernel_ldst_body(a, sig);
@@ -131,18 +137,22 @@ __global__ void __launch_bounds__(kLdstThreads) gather_kernel_ldst(const __grid_
 }
 
 // ------------------------------------------------------------------ tma engine
-// The part of piece s the bulk engine takes: both ends 16-byte aligned.
-__device__ __forceinline__ bool bulk_part(const GatherArgs &a, int r, int s, int64_t x0, int64_t x1,
-                                          int64_t &p0, int64_t &pend, int64_t &d0)
+// The part of piece s the bulk engine takes: shard bytes [p0, pend), both
+// ends 16-byte aligned on both sides.
+template <class Args>
+__device__ __forceinline__ bool bulk_part(const Args &a, int r, int s, int64_t x0, int64_t x1,
+                                          int64_t &p0, int64_t &pend)
 {
     int64_t p1;
-    if (!piece_of(a, r, s, x0, x1, p0, p1, d0)) return false;
-    if ((p0 & 15) || (d0 & 15)) return false;
+    if (!piece_of(a, s, x0, x1, p0, p1)) return false;
+    if ((((uint64_t)(uintptr_t)a.src[r] + (uint64_t)p0) & 15) || (slot_offset(a, r, s, p0) & 15))
+        return false;
     pend = p0 + ((p1 - p0) & ~(int64_t)15);
     return pend > p0;
 }
 
-__device__ __forceinline__ void gather_kernel_tma_body(const GatherArgs &a, const SignalArgs &sig)
+template <class Args>
+__device__ __forceinline__ void gather_kernel_tma_body(const Args &a, const SignalArgs &sig)
 {
     extern __shared__ __align__(128) unsigned char stage_mem[];
     __shared__ __align__(8) uint64_t full[kTmaStages];
@@ -154,33 +164,34 @@ __device__ __forceinline__ void gather_kernel_tma_body(const GatherArgs &a, cons
     const char *src = static_cast<const char *>(a.src[r]);
     const int sfirst = x0 < x1 ? first_split_after(a, x0) : a.nsplit;
 
-    // Chunk iterator over the bulk parts of the region's pieces (thread 0).
+    // Chunk iterator over the bulk parts of the region's pieces (thread 0):
+    // shard byte position, split and length of the next chunk.
     int s = sfirst - 1;
-    int64_t pos = 0, pend = 0, dpos = 0;
-    auto next = [&](int64_t &cs, int64_t &cd, uint32_t &cl) -> bool {
+    int64_t pos = 0, pend = 0;
+    auto next = [&](int64_t &cs, int &csplit, uint32_t &cl) -> bool {
         while (pos >= pend) {
             ++s;
             if (s >= a.nsplit || a.off[s] >= x1) return false;
-            int64_t p0, pe, d0;
-            if (bulk_part(a, r, s, x0, x1, p0, pe, d0)) {
+            int64_t p0, pe;
+            if (bulk_part(a, r, s, x0, x1, p0, pe)) {
                 pos = p0;
                 pend = pe;
-                dpos = d0;
             }
         }
         const int64_t left = pend - pos;
         cl = (uint32_t)(left < kTmaChunk ? left : kTmaChunk);
         cs = pos;
-        cd = dpos;
+        csplit = s;
         pos += cl;
-        dpos += cl;
         return true;
     };
-    int64_t dst_of[kTmaStages];
+    int64_t pos_of[kTmaStages];
+    int split_of[kTmaStages];
     uint32_t len_of[kTmaStages];
-    auto issue = [&](int k, int64_t cs, int64_t cd, uint32_t cl) {
+    auto issue = [&](int k, int64_t cs, int csplit, uint32_t cl) {
         const int st = k % kTmaStages;
-        dst_of[st] = cd;
+        pos_of[st] = cs;
+        split_of[st] = csplit;
         len_of[st] = cl;
         mbar_expect_tx(&full[st], cl);
         bulk_load(stage_mem + (size_t)st * kTmaChunk, src + cs, cl, &full[st]);
@@ -199,9 +210,10 @@ __device__ __forceinline__ void gather_kernel_tma_body(const GatherArgs &a, cons
     if (threadIdx.x == 0) {
         for (int i = 0; i < kTmaStages; ++i) mbar_init(&full[i], 1);
         fence_mbar_init();
-        int64_t cs, cd;
+        int64_t cs;
+        int csplit;
         uint32_t cl;
-        while (nissued < kTmaStages && next(cs, cd, cl)) issue(nissued++, cs, cd, cl);
+        while (nissued < kTmaStages && next(cs, csplit, cl)) issue(nissued++, cs, csplit, cl);
     }
     if (b == 0) emit(sig, RR_BARRIER_ARRIVE, r, 0);
     else __syncthreads();
@@ -214,12 +226,12 @@ __device__ __forceinline__ void gather_kernel_tma_body(const GatherArgs &a, cons
         // Everything the bulk engine does not take.
         const int tid = threadIdx.x - 32, nthr = kTmaThreads - 32;
         for (int sp = sfirst; sp < a.nsplit && a.off[sp] < x1; ++sp) {
-            int64_t p0, p1, d0, q0, qend, e0;
-            if (!piece_of(a, r, sp, x0, x1, p0, p1, d0)) continue;
-            if (bulk_part(a, r, sp, x0, x1, q0, qend, e0))
-                push_bytes(a, src + qend, d0 + (qend - p0), p1 - qend, tid, nthr);
+            int64_t p0, p1, q0, qend;
+            if (!piece_of(a, sp, x0, x1, p0, p1)) continue;
+            if (bulk_part(a, r, sp, x0, x1, q0, qend))
+                push_bytes(a, r, sp, src, qend, p1 - qend, tid, nthr);
             else
-                push_bytes(a, src + p0, d0, p1 - p0, tid, nthr);
+                push_bytes(a, r, sp, src, p0, p1 - p0, tid, nthr);
         }
     } else if (threadIdx.x == 0) {
         bool ok = true;
@@ -232,15 +244,16 @@ __device__ __forceinline__ void gather_kernel_tma_body(const GatherArgs &a, cons
             }
             fence_async_shared();
             for (int q = 0; q < a.nout; ++q)
-                bulk_store(static_cast<char *>(a.out[a.qlist[q]]) + dst_of[st],
-                           stage_mem + (size_t)st * kTmaChunk, len_of[st]);
+                bulk_store(slot_dst(a, q, r, split_of[st], pos_of[st]), stage_mem + (size_t)st * kTmaChunk,
+                           len_of[st]);
             bulk_commit();
             if (k >= 1) {
-                int64_t cs, cd;
+                int64_t cs;
+                int csplit;
                 uint32_t cl;
-                if (next(cs, cd, cl)) {
+                if (next(cs, csplit, cl)) {
                     bulk_wait_read_1();  // chunk k-1's stores have read their stage
-                    issue(nissued++, cs, cd, cl);
+                    issue(nissued++, cs, csplit, cl);
                 }
             }
         }
@@ -252,17 +265,23 @@ __device__ __forceinline__ void gather_kernel_tma_body(const GatherArgs &a, cons
     wait(sig, RR_BARRIER_END, r, b, &s_ok);
 }
 
-__global__ void __launch_bounds__(kTmaThreads) gather_kernel_tma(const __grid_constant__ GatherArgs a)
+template <class Args>
+__global__ void __launch_bounds__(kTmaThreads) gather_kernel_tma(const __grid_constant__ Args a)
 {
     const SignalArgs sig = begin_call(a.sig);
     gather_kernel_tma_body(a, sig);
     end_call(sig);
 }
 
-KernelChoice gather_kernel_for(int engine)
+KernelChoice gather_kernel_for(int engine, bool list)
 {
-    if (engine == 2) return KernelChoice{(const void *)gather_kernel_tma, kTmaThreads, kTmaSmem};
-    return KernelChoice{(const void *)gather_kernel_ldst, kLdstThreads, 0};
+    if (engine == 2)
+        return KernelChoice{list ? (const void *)gather_kernel_tma<GatherListArgs>
+                                 : (const void *)gather_kernel_tma<GatherArgs>,
+                            kTmaThreads, kTmaSmem};
+    return KernelChoice{list ? (const void *)gather_kernel_ldst<GatherListArgs>
+                             : (const void *)gather_kernel_ldst<GatherArgs>,
+                        kLdstThreads, 0};
 }
 
 }  // namespace rr

@@ -30,7 +30,7 @@ struct rr_signal_pad {
     int64_t round_bytes;  // 0 = automatic
     int inject;        // -1 or rank*4 + barrier
     int blocks_override;
-    int engine;        // gathers: 0 auto, 1 ldst, 2 tma
+    int engine;        // gathers: 0 auto, 1 ldst, 2 tma, 3 copy engines
     int reduce_engine; // one-shot with copy_mode off: 0 auto, 1 ldst, 2 tma
     int twoshot_mode;  // 0 auto, 1 pull (middle barrier), 2 push (owner broadcasts)
     int last_grid;
@@ -351,9 +351,10 @@ rr_status allreduce_common(bool twoshot, const void *const *inputs, void *const 
     return launch(pad, k, W * B, a, stream);
 }
 
-rr_status gather_common(const void *const *rank_bufs, void *const *outputs, int W,
-                        const int64_t *splits, int nsplit, rr_dtype dtype, rr_signal_pad *pad,
-                        cudaStream_t stream)
+// Checks shared by every gather: pad, dtype, split table (-> a.off, in
+// bytes), rank buffers.  *shard = bytes per rank.
+rr_status gather_prepare(const void *const *rank_bufs, int W, const int64_t *splits, int nsplit,
+                         rr_dtype dtype, rr_signal_pad *pad, rr::GatherArgs &a, int64_t *shard)
 {
     rr_status st = check_pad(pad, W);
     if (st != RR_OK) return st;
@@ -362,9 +363,7 @@ rr_status gather_common(const void *const *rank_bufs, void *const *outputs, int 
     if (nsplit < 0 || nsplit > RR_MAX_SPLITS)
         return fail(RR_ERR_INVALID_ARG, "num_splits %d outside 0..%d", nsplit, RR_MAX_SPLITS);
     if (nsplit > 0 && !splits) return fail(RR_ERR_INVALID_ARG, "split_sizes is NULL");
-    if (!rank_bufs || !outputs) return fail(RR_ERR_INVALID_ARG, "rank_bufs / outputs array is NULL");
-    rr::GatherArgs a;
-    std::memset(&a, 0, sizeof a);
+    if (!rank_bufs) return fail(RR_ERR_INVALID_ARG, "rank_bufs array is NULL");
     int64_t total = 0;
     a.off[0] = 0;
     for (int s = 0; s < nsplit; ++s) {
@@ -373,18 +372,74 @@ rr_status gather_common(const void *const *rank_bufs, void *const *outputs, int 
         if (total > ((int64_t)1 << 40)) return fail(RR_ERR_INVALID_ARG, "shard too large");
         a.off[s + 1] = total * eb;
     }
-    const int64_t shard = total * eb;
-    const int64_t outb = shard * W;
-    int nout = 0;
     for (int r = 0; r < W; ++r) {
         if (!rank_bufs[r]) return fail(RR_ERR_INVALID_ARG, "rank_bufs[%d] is NULL", r);
         if (!aligned16(rank_bufs[r])) return fail(RR_ERR_ALIGNMENT, "rank_bufs[%d] not 16-byte aligned", r);
+        a.src[r] = rank_bufs[r];
+    }
+    a.W = W;
+    a.nsplit = nsplit;
+    *shard = total * eb;
+    return RR_OK;
+}
+
+// Enqueue a gather whose arguments are complete but for B and the signal
+// arguments.  Engine 3 (copy engines) issues one cudaMemcpyAsync per
+// (materialised output, rank, param) slot instead of a kernel: stream order
+// stands in for the barriers, since on one GPU the copies start after
+// whatever wrote the shards and end before whatever reads the outputs.
+template <class Args>
+rr_status run_gather(rr_signal_pad *pad, Args &a, int64_t shard, bool list, cudaStream_t stream)
+{
+    rr_status st = check_device(pad);
+    if (st != RR_OK) return st;
+    const int engine = pad->engine == 0 ? 2 : pad->engine;
+    if (engine == 3) {
+        for (int q = 0; q < a.nout; ++q)
+            for (int r = 0; r < a.W; ++r)
+                for (int s = 0; s < a.nsplit; ++s) {
+                    const int64_t o = a.off[s], len = a.off[s + 1] - o;
+                    if (len == 0) continue;
+                    cudaError_t e = cudaMemcpyAsync(rr::slot_dst(a, q, r, s, o),
+                                                    static_cast<const char *>(a.src[r]) + o, (size_t)len,
+                                                    cudaMemcpyDeviceToDevice, stream);
+                    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+                }
+        pad->last_grid = 0;
+        pad->last_B = 0;
+        pad->last_engine = 3;
+        return ok();
+    }
+    const rr::KernelChoice k = rr::gather_kernel_for(engine, list);
+    int B = 0;
+    st = plan_blocks(pad, k, a.W, shard * a.W + shard * a.W * a.nout, &B);
+    if (st != RR_OK) return st;
+    a.B = B;
+    a.sig = signal_args(pad);
+    pad->last_B = B;
+    pad->last_engine = engine;
+    return launch(pad, k, a.W * B, a, stream);
+}
+
+rr_status gather_common(const void *const *rank_bufs, void *const *outputs, int W,
+                        const int64_t *splits, int nsplit, rr_dtype dtype, rr_signal_pad *pad,
+                        cudaStream_t stream)
+{
+    rr::GatherArgs a;
+    std::memset(&a, 0, sizeof a);
+    int64_t shard = 0;
+    rr_status st = gather_prepare(rank_bufs, W, splits, nsplit, dtype, pad, a, &shard);
+    if (st != RR_OK) return st;
+    if (!outputs) return fail(RR_ERR_INVALID_ARG, "outputs array is NULL");
+    const int64_t outb = shard * W;
+    for (int r = 0; r < W; ++r) {
         if (outputs[r]) {
             if (!aligned16(outputs[r])) return fail(RR_ERR_ALIGNMENT, "outputs[%d] not 16-byte aligned", r);
-            ++nout;
+            a.out[r] = outputs[r];
+            a.qlist[a.nout++] = r;
         }
     }
-    if (nout == 0) return fail(RR_ERR_INVALID_ARG, "no output is materialised");
+    if (a.nout == 0) return fail(RR_ERR_INVALID_ARG, "no output is materialised");
     for (int i = 0; i < W; ++i) {
         if (!outputs[i]) continue;
         const Span oi = span_of(outputs[i], outb);
@@ -396,26 +451,47 @@ rr_status gather_common(const void *const *rank_bufs, void *const *outputs, int 
         }
     }
     if (shard == 0) return ok();
-    st = check_device(pad);
-    if (st != RR_OK) return st;
+    return run_gather(pad, a, shard, false, stream);
+}
 
-    const int engine = pad->engine == 0 ? 2 : pad->engine;
-    const rr::KernelChoice k = rr::gather_kernel_for(engine);
-    int B = 0;
-    st = plan_blocks(pad, k, W, shard * W + shard * W * nout, &B);
+rr_status gather_list_impl(const void *const *rank_bufs, void *const *out_lists, int W, int64_t numel,
+                           rr_dtype dtype, rr_signal_pad *pad, cudaStream_t stream)
+{
+    if (numel < 0) return fail(RR_ERR_INVALID_ARG, "numel_per_rank %lld", (long long)numel);
+    rr::GatherListArgs a;
+    std::memset(&a, 0, sizeof a);
+    int64_t shard = 0;
+    rr_status st = gather_prepare(rank_bufs, W, &numel, 1, dtype, pad, a, &shard);
     if (st != RR_OK) return st;
-    for (int r = 0; r < W; ++r) {
-        a.src[r] = rank_bufs[r];
-        a.out[r] = outputs[r];
-        if (outputs[r]) a.qlist[a.nout++] = r;
+    if (!out_lists) return fail(RR_ERR_INVALID_ARG, "output list array is NULL");
+    for (int q = 0; q < W; ++q) {
+        int set = 0;
+        for (int r = 0; r < W; ++r) {
+            void *p = out_lists[q * W + r];
+            if (!p) continue;
+            if (!aligned16(p)) return fail(RR_ERR_ALIGNMENT, "output list %d entry %d not 16-byte aligned", q, r);
+            a.lst[q * W + r] = p;
+            ++set;
+        }
+        if (set != 0 && set != W)
+            return fail(RR_ERR_INVALID_ARG, "output list %d has %d of %d buffers (all or none)", q, set, W);
+        if (set) a.qlist[a.nout++] = q;
     }
-    a.W = W;
-    a.B = B;
-    a.nsplit = nsplit;
-    a.sig = signal_args(pad);
-    pad->last_B = B;
-    pad->last_engine = engine;
-    return launch(pad, k, W * B, a, stream);
+    if (a.nout == 0) return fail(RR_ERR_INVALID_ARG, "no output is materialised");
+    // Every list buffer against every other one and every rank buffer.
+    for (int i = 0; i < W * W; ++i) {
+        if (!a.lst[i]) continue;
+        const Span si = span_of(a.lst[i], shard);
+        for (int j = i + 1; j < W * W; ++j)
+            if (a.lst[j] && overlaps(si, span_of(a.lst[j], shard)))
+                return fail(RR_ERR_ALIAS, "output list %d entry %d and list %d entry %d overlap", i / W, i % W,
+                            j / W, j % W);
+        for (int r = 0; r < W; ++r)
+            if (overlaps(si, span_of(rank_bufs[r], shard)))
+                return fail(RR_ERR_ALIAS, "output list %d entry %d and rank_bufs[%d] overlap", i / W, i % W, r);
+    }
+    if (shard == 0) return ok();
+    return run_gather(pad, a, shard, true, stream);
 }
 
 }  // namespace
@@ -529,7 +605,7 @@ rr_status rr_signal_pad_set_option(rr_signal_pad *pad, rr_option opt, int64_t va
         pad->blocks_override = (int)value;
         return ok();
     case RR_OPT_GATHER_ENGINE:
-        if (value < 0 || value > 2) return fail(RR_ERR_INVALID_ARG, "engine %lld", (long long)value);
+        if (value < 0 || value > 3) return fail(RR_ERR_INVALID_ARG, "gather engine %lld", (long long)value);
         pad->engine = (int)value;
         return ok();
     case RR_OPT_INJECT_SKIP:
@@ -636,6 +712,12 @@ rr_status rr_allgather_param_contiguous(const void *const *rank_bufs, void *cons
                                         rr_dtype dtype, rr_signal_pad *pad, cudaStream_t stream)
 {
     return gather_common(rank_bufs, outputs, world_size, split_sizes, num_splits, dtype, pad, stream);
+}
+
+rr_status rr_allgather_list(const void *const *rank_bufs, void *const *output_lists, int world_size,
+                            int64_t numel_per_rank, rr_dtype dtype, rr_signal_pad *pad, cudaStream_t stream)
+{
+    return gather_list_impl(rank_bufs, output_lists, world_size, numel_per_rank, dtype, pad, stream);
 }
 
 const char *rr_status_string(rr_status s)

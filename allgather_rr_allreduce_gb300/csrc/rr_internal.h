@@ -81,6 +81,33 @@ struct GatherArgs {
     SignalArgs sig;
 };
 
+// List-output allgather (torch.distributed.all_gather): output q is W
+// separate buffers, lst[q*W + r] receiving rank r's shard.  Always one split;
+// out[] is unused.
+struct GatherListArgs : GatherArgs {
+    void *lst[RR_MAX_WORLD * RR_MAX_WORLD];
+};
+
+// Byte offset, inside its destination buffer, of byte p0 (in split s) of
+// rank r's shard.  Param-contiguous: O_s*W + r*E_s + (p0 - O_s), in bytes.
+// List output: each rank has a buffer of its own, so the shard's own offset.
+RR_HD int64_t slot_offset(const GatherArgs &a, int r, int s, int64_t p0)
+{
+    const int64_t o = a.off[s], e = a.off[s + 1];
+    return o * a.W + (int64_t)r * (e - o) + (p0 - o);
+}
+RR_HD int64_t slot_offset(const GatherListArgs &, int, int, int64_t p0) { return p0; }
+
+// Address of that byte in the q-th materialised output (qlist order).
+RR_HD char *slot_dst(const GatherArgs &a, int q, int r, int s, int64_t p0)
+{
+    return static_cast<char *>(a.out[a.qlist[q]]) + slot_offset(a, r, s, p0);
+}
+RR_HD char *slot_dst(const GatherListArgs &a, int q, int r, int, int64_t p0)
+{
+    return static_cast<char *>(a.lst[a.qlist[q] * a.W + r]) + p0;
+}
+
 // ---------------------------------------------------------------- partition
 // Work is cut into 256-byte granules (16 vectors of 16 bytes) so that block
 // boundaries never split a 128-byte line between two blocks.
@@ -147,6 +174,6 @@ KernelChoice twoshot_kernel_for(rr_dtype dtype, int W, bool copy_mode, bool push
 KernelChoice oneshot_tma_kernel_for(rr_dtype dtype, int W);  // copy_mode off, bulk-copy loads
 // copy_mode on, staging by a bulk-copy producer warp (two-shot: push allgather)
 KernelChoice staged_kernel_for(rr_dtype dtype, int W, bool twoshot);
-KernelChoice gather_kernel_for(int engine);  // 1 = loads/stores, 2 = TMA bulk
+KernelChoice gather_kernel_for(int engine, bool list);  // 1 = loads/stores, 2 = TMA bulk
 
 }  // namespace rr

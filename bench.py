@@ -374,6 +374,89 @@ def fsdp_28_layers(rr, stream):
             "pct_of_8TBps": round(100 * total / ms / 1e6 / NOMINAL_HBM_GBS, 2)}
 
 
+def overlap_gemm(rr, stream, n_ag=40, mkn=8192):
+    """Rank-major allgather (W=8, 32 MiB bf16 per rank, rank 0's output) on
+    every gather engine, alone and while cuBLAS bf16 GEMMs (mkn^3) run on a
+    second stream: does the gather slow down when it shares the GPU with
+    compute, and by how much does it slow the GEMMs?  The copy engines take
+    no SM.  Per engine: n_ag gathers; the GEMM count is chosen so that both
+    streams are busy for about the same time."""
+    n = N
+    g = torch.Generator(device="cuda").manual_seed(workloads.LARGE["seed_base"] + 5)
+    x = torch.randn((W, n), generator=g, device="cuda").to(torch.bfloat16)
+    y = torch.empty(W * n, dtype=torch.bfloat16, device="cuda")
+    a = torch.randn((mkn, mkn), generator=g, device="cuda").to(torch.bfloat16)
+    b = torch.randn((mkn, mkn), generator=g, device="cuda").to(torch.bfloat16)
+    c = torch.empty((mkn, mkn), dtype=torch.bfloat16, device="cuda")
+    gs = torch.cuda.Stream()
+    pad = rr.rr_signal_pad_create(W)
+    call = rr.bound_call("rr_allgather", [x[r].data_ptr() for r in range(W)],
+                         [y.data_ptr()] + [None] * (W - 1), W, n, rr.RR_BF16, pad, stream.cuda_stream)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    def gemm():
+        with torch.cuda.stream(gs):
+            torch.matmul(a, b, out=c)
+
+    def span(st, fn, k):
+        e0, e1 = ev(), ev()
+        e0.record(st)
+        for _ in range(k):
+            fn()
+        e1.record(st)
+        e1.synchronize()
+        return e0.elapsed_time(e1)
+
+    for _ in range(3):
+        gemm()
+    gemm_ms = span(gs, gemm, 10) / 10
+    out = {"bytes_per_call": 2 * W * n * EB, "gemm": f"bf16 {mkn}x{mkn}x{mkn} (cuBLAS via torch.matmul)",
+           "gemm_alone_us": round(1000 * gemm_ms, 1), "engines": {}}
+    for name, code in (("ldst", 1), ("tma", 2), ("copy_engine", 3)):
+        pad.set_option("gather_engine", code)
+        for _ in range(5):
+            call()
+        stream.synchronize()
+        ag_ms = span(stream, call, n_ag) / n_ag
+        n_gemm = max(1, round(n_ag * ag_ms / gemm_ms))
+        # both streams start together behind one event, issue interleaved
+        torch.cuda.synchronize()
+        go = ev()
+        go.record(stream)
+        gs.wait_event(go)
+        a0, a1, g0, g1 = ev(), ev(), ev(), ev()
+        a0.record(stream)
+        g0.record(gs)
+        ratio = n_ag / n_gemm
+        issued = 0
+        for i in range(n_gemm):
+            gemm()
+            while issued < round((i + 1) * ratio):
+                call()
+                issued += 1
+        while issued < n_ag:
+            call()
+            issued += 1
+        a1.record(stream)
+        g1.record(gs)
+        torch.cuda.synchronize()
+        ag_with = a0.elapsed_time(a1) / n_ag
+        gemm_with = g0.elapsed_time(g1) / n_gemm
+        makespan = max(go.elapsed_time(a1), go.elapsed_time(g1))
+        serial = n_ag * ag_ms + n_gemm * gemm_ms
+        out["engines"][name] = {
+            "ag_alone_us": round(1000 * ag_ms, 1), "ag_with_gemm_us": round(1000 * ag_with, 1),
+            "ag_slowdown": round(ag_with / ag_ms, 3), "gemms": n_gemm,
+            "gemm_with_ag_us": round(1000 * gemm_with, 1), "gemm_slowdown": round(gemm_with / gemm_ms, 3),
+            "makespan_ms": round(makespan, 3), "serial_ms": round(serial, 3),
+            "overlap_gain": round(serial / makespan, 3)}
+    pad.status(stream)
+    pad.close()
+    return out
+
+
 def run_gpu(args, rank, world, local_rank):
     import allgather_rr_allreduce_gb300 as rr
     from allgather_rr_allreduce_gb300 import build as rr_build
@@ -474,6 +557,7 @@ def run_gpu(args, rank, world, local_rank):
     if not args.no_extras:
         extras["latency_us"] = latency_sweep(rr, stream)
         extras["fsdp_28_layers"] = fsdp_28_layers(rr, stream)
+        extras["overlap_gemm"] = overlap_gemm(rr, stream)
 
     line = {
         "metric": METRIC,
@@ -605,7 +689,8 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("rr", "reference"), default="rr")
-    ap.add_argument("--no-extras", action="store_true", help="skip the latency sweep and the 28-layer run")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the latency sweep, the 28-layer run and the GEMM-overlap run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="", help="comma-separated subset of ops (profiling runs)")
     ap.add_argument("--numel", type=int, default=0, help="elements per rank for the allreduce/allgather ops")

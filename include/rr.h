@@ -78,7 +78,15 @@ typedef enum {
 typedef enum {
     RR_OPT_TIMEOUT_NS = 0,      /* barrier wait limit in ns (default 2e9) */
     RR_OPT_BLOCKS_PER_RANK = 1, /* 0 = automatic (default); else a fixed block count per rank */
-    RR_OPT_GATHER_ENGINE = 2,   /* 0 = automatic, 1 = 128-bit loads/stores, 2 = TMA bulk copies */
+    RR_OPT_GATHER_ENGINE = 2,   /* 0 = automatic (TMA bulk copies), 1 = 128-bit loads/stores,
+                                   2 = TMA bulk copies, 3 = the GPU's copy engines: one
+                                   cudaMemcpyAsync per (output, rank, param) slot and no
+                                   kernel, so no SM is taken from concurrent compute
+                                   ("ccl: hierarchical cross-node AllGather (intra-node SDMA
+                                   + inter-node RDMA) #441", PR description: the intra-node
+                                   gather on copy engines overlaps a concurrent GEMM).  The
+                                   copies are ordered by the stream alone: they pass no
+                                   barrier and ignore a pending timeout on the pad */
     RR_OPT_INJECT_SKIP = 3,     /* fault injection: -1 = off; else rank*4 + barrier: that rank
                                    never emits that barrier's flags, so peers time out */
     RR_OPT_ROUND_BYTES = 4,     /* bytes per rank per round of a pipelined chunk (copy_mode
@@ -104,7 +112,8 @@ typedef enum {
                                    mode: reads the device counter, synchronising the device) */
     RR_OPT_LAST_GRID = 17,      /* blocks launched by the last call */
     RR_OPT_LAST_BLOCKS_PER_RANK = 18,
-    RR_OPT_LAST_ENGINE = 19,    /* engine the last call used (1 = loads/stores, 2 = bulk copies) */
+    RR_OPT_LAST_ENGINE = 19,    /* engine the last call used (1 = loads/stores, 2 = bulk copies,
+                                   3 = copy engines) */
     RR_OPT_WORLD_SIZE = 20,
     RR_OPT_MAX_BLOCKS_PER_RANK = 21
 } rr_option;
@@ -269,6 +278,28 @@ rr_status rr_allgather_param_contiguous(const void *const *rank_bufs, void *cons
                                         int world_size, const int64_t *split_sizes,
                                         int num_splits, rr_dtype dtype, rr_signal_pad *pad,
                                         cudaStream_t stream);
+
+/*
+ * rr_allgather_list -- torch.distributed.all_gather with list output: output
+ * q is a list of W separate buffers, and buffer r of every materialised list
+ * receives rank r's shard.
+ *
+ * Source: "ccl: hierarchical cross-node AllGather (intra-node SDMA +
+ * inter-node RDMA) #441", the commit adding HierAllGather.all_gather
+ * (tensor_list, tensor) on the same path as all_gather_into_tensor, bit-exact
+ * against torch for bf16/fp16/fp32/int32.  The same kernels as rr_allgather
+ * run it (one launch); only each slot's destination differs.
+ *
+ * rank_bufs:    W device pointers, rank r's shard (numel_per_rank elements).
+ * output_lists: HOST array of W*W device pointers; entry q*W + r is buffer r
+ *               of rank q's list (numel_per_rank elements).  Row q is either
+ *               all non-NULL (materialised) or all NULL; at least one row is
+ *               materialised.  No buffer may overlap another or a rank buffer.
+ * Raw bits are copied.  Barriers: ARRIVE, END (none with the copy engines).
+ */
+rr_status rr_allgather_list(const void *const *rank_bufs, void *const *output_lists, int world_size,
+                            int64_t numel_per_rank, rr_dtype dtype, rr_signal_pad *pad,
+                            cudaStream_t stream);
 
 /*
  * rr_allreduce_oneshot_noalloc -- rr_allreduce_oneshot for callers that may

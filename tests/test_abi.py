@@ -31,7 +31,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for must in ("rr_allreduce_oneshot", "rr_allreduce_twoshot", "rr_allgather",
-                 "rr_allgather_param_contiguous", "rr_signal_pad_create"):
+                 "rr_allgather_param_contiguous", "rr_allgather_list", "rr_signal_pad_create"):
         assert must in names
 
 
@@ -65,6 +65,8 @@ def test_host_argument_checks_without_a_gpu(rr):
     assert lib.rr_allgather(arr, arr, 2, 8, 0, None, None) == rr.RR_ERR_INVALID_ARG
     sp = (ctypes.c_int64 * 1)(8)
     assert lib.rr_allgather_param_contiguous(arr, arr, 2, sp, 1, 0, None, None) == rr.RR_ERR_INVALID_ARG
+    lists = rr.pointer_array([16, 32, 48, 64])
+    assert lib.rr_allgather_list(arr, lists, 2, 8, 0, None, None) == rr.RR_ERR_INVALID_ARG
     assert lib.rr_signal_pad_status(None, None) == rr.RR_ERR_INVALID_ARG
     assert lib.rr_signal_pad_set_option(None, 0, 1) == rr.RR_ERR_INVALID_ARG
     assert lib.rr_signal_pad_destroy(None) == rr.RR_OK

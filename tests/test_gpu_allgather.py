@@ -1,7 +1,7 @@
-"""GPU parity: rank-major and param-contiguous allgather through the C ABI,
-bit for bit against the CPU oracle, on both copy engines (128-bit
-loads/stores and TMA bulk copies).  Random-bit inputs carry NaN and Inf
-encodings, which must survive untouched."""
+"""GPU parity: rank-major, list-output and param-contiguous allgather
+through the C ABI, bit for bit against the CPU oracle, on every engine
+(128-bit loads/stores, TMA bulk copies, the GPU's copy engines).  Random-bit
+inputs carry NaN and Inf encodings, which must survive untouched."""
 import numpy as np
 import pytest
 import torch
@@ -12,7 +12,7 @@ from gpu_util import GuardedOutputs, RankBuffers, assert_bitwise
 
 pytestmark = pytest.mark.gpu
 
-ENGINES = {"ldst": 1, "tma": 2}
+ENGINES = {"ldst": 1, "tma": 2, "copy_engine": 3}
 
 
 @pytest.fixture(scope="module")
@@ -225,3 +225,120 @@ def test_gather_argument_errors(rr):
         rr.rr_allgather(bufs.ptrs, [outs.ptrs[0] + 4, None, None, None], W, N, "fp32", pad)
     assert e.value.status == rr.RR_ERR_ALIGNMENT
     pad.status()
+
+
+LIST_SHAPES = [(2, 4096), (3, 1001), (8, 8195), (16, 2048), (8, 1), (5, 77_777)]
+
+
+class ListOutputs:
+    """W lists of W device buffers (row q = rank q's all_gather tensor_list),
+    every buffer a separate slice of one arena with canaries on both sides
+    and a ragged lead, so that no buffer sits at an allocation's base and
+    the rows are not laid out rank-major."""
+
+    def __init__(self, W, n, dtype, materialise=None):
+        eb = workloads.ELEM_BYTES[dtype]
+        self.W, self.n, self.dtype, self.eb = W, n, dtype, eb
+        self.rows = set(range(W)) if materialise is None else set(materialise)
+        self.stride = ((n * eb + 15) // 16) * 16 + 2 * 256
+        self.arena = torch.full((W * W * self.stride + 4096,), 0xA5, dtype=torch.uint8, device="cuda")
+        base = self.arena.data_ptr()
+        # buffer (q, r) sits at slot (r * W + q) reversed: column-major and backwards
+        self.off = {}
+        for q in range(W):
+            for r in range(W):
+                slot = W * W - 1 - (r * W + q)
+                self.off[(q, r)] = 2048 + slot * self.stride + 256
+        self.lists = [[base + self.off[(q, r)] for r in range(W)] if q in self.rows else None
+                      for q in range(W)]
+
+    def host(self, q, r):
+        o = self.off[(q, r)]
+        t = self.arena[o:o + self.n * self.eb]
+        return t.cpu().numpy().view(workloads.STORAGE[self.dtype])
+
+    def check_guards(self):
+        a = self.arena.cpu().numpy()
+        used = np.zeros(a.size, dtype=bool)
+        for q in self.rows:
+            for r in range(self.W):
+                o = self.off[(q, r)]
+                used[o:o + self.n * self.eb] = True
+        assert np.all(a[~used] == 0xA5), "a byte outside the list buffers was written"
+
+
+@pytest.mark.parametrize("engine", list(ENGINES))
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32", "int32"])
+@pytest.mark.parametrize("W,N", LIST_SHAPES, ids=[f"W{w}_N{n}" for w, n in LIST_SHAPES])
+def test_list_output_matches_oracle(rr, engine, dtype, W, N):
+    """torch.distributed.all_gather semantics: buffer r of every list holds
+    rank r's shard, i.e. slice r of the oracle's rank-major output."""
+    ins = workloads.rank_buffers(W, N, dtype, "bits", seed_base=70 * W + N % 97)
+    want = oracle.allgather_rank_major(ins, dtype)
+    pad = pad_for(rr, W)
+    pad.set_option("gather_engine", ENGINES[engine])
+    bufs = RankBuffers(W, N, dtype)
+    bufs.fill(ins)
+    materialise = (0,) if W == 16 else None
+    outs = ListOutputs(W, N, dtype, materialise=materialise)
+    rr.rr_allgather_list(bufs.ptrs, outs.lists, W, N, dtype, pad)
+    pad.status()
+    assert pad.get_option("last_engine") == ENGINES[engine]
+    for q in sorted(outs.rows):
+        for r in range(W):
+            assert_bitwise(outs.host(q, r), want[r * N:(r + 1) * N], f"list {q} buffer {r}")
+    outs.check_guards()
+
+
+def test_list_output_argument_errors(rr):
+    W, N = 4, 1024
+    pad = pad_for(rr, W)
+    pad.set_option("gather_engine", 0)
+    bufs = RankBuffers(W, N, "fp32")
+    outs = ListOutputs(W, N, "fp32")
+    half = [outs.lists[0][:2] + [None, None]] + outs.lists[1:]
+    with pytest.raises(rr.RRError) as e:
+        rr.rr_allgather_list(bufs.ptrs, half, W, N, "fp32", pad)
+    assert e.value.status == rr.RR_ERR_INVALID_ARG
+    with pytest.raises(rr.RRError) as e:
+        rr.rr_allgather_list(bufs.ptrs, [None] * W, W, N, "fp32", pad)
+    assert e.value.status == rr.RR_ERR_INVALID_ARG
+    dup = [list(row) for row in outs.lists]
+    dup[2][3] = dup[1][0]
+    with pytest.raises(rr.RRError) as e:
+        rr.rr_allgather_list(bufs.ptrs, dup, W, N, "fp32", pad)
+    assert e.value.status == rr.RR_ERR_ALIAS
+    onto_shard = [list(row) for row in outs.lists]
+    onto_shard[0][1] = bufs.ptrs[3]
+    with pytest.raises(rr.RRError) as e:
+        rr.rr_allgather_list(bufs.ptrs, onto_shard, W, N, "fp32", pad)
+    assert e.value.status == rr.RR_ERR_ALIAS
+    odd = [list(row) for row in outs.lists]
+    odd[3][2] = odd[3][2] + 4
+    with pytest.raises(rr.RRError) as e:
+        rr.rr_allgather_list(bufs.ptrs, odd, W, N, "fp32", pad)
+    assert e.value.status == rr.RR_ERR_ALIGNMENT
+    # nothing was written by the rejected calls
+    a = outs.arena.cpu().numpy()
+    assert np.all(a == 0xA5)
+    pad.status()
+
+
+@pytest.mark.parametrize("engine", list(ENGINES))
+def test_engines_agree_on_the_fsdp_layer_and_the_list(rr, engine):
+    """Every engine, given the same shards, writes the same bytes as the
+    oracle into a param-contiguous output and into list outputs, back to
+    back on one pad (the copy engines leave the pad's generation as it
+    was, the kernels advance it)."""
+    W, dtype = 8, "bf16"
+    splits = [4096, 512, 512, 4096, 9, 8 * 2368, 8 * 2368]
+    ins = workloads.rank_buffers(W, sum(splits), dtype, "bits", seed_base=77)
+    want = oracle.allgather_param_contiguous(ins, splits, dtype)
+    pad = pad_for(rr, W)
+    g0 = pad.get_option("generation")
+    _, outs = gather(rr, W, dtype, ins, splits=splits, engine=engine, materialise=(1, 6))
+    g1 = pad.get_option("generation")
+    assert (g1 == g0) if engine == "copy_engine" else (g1 != g0)
+    for q in (1, 6):
+        assert_bitwise(outs.host(q), want, f"output {q}")
+    outs.check_guards()
