@@ -183,13 +183,61 @@ __device__ __forceinline__ bool wait_round(const SignalArgs &s, int kind, int r,
     return wait_on(s, round_barrier(kind), r, b,
                    [&](int p) { return (int64_t)(ld_flag64_acquire(slots + p) - target) >= 0; }, s_ok, sync);
 }
-// Round flag k from a single thread (the producer lane of a warp-specialised
-// block): stores to all W listeners.  The caller has made the round's data
-// visible (bulk-store completion and an async-proxy fence).
+// Round flags up to round k from a single thread (the producer lane of a
+// warp-specialised block): one release fence, then relaxed stores of the
+// newest value to all W listeners.  Waits accept any value at or past their
+// target, so publishing round k also publishes every earlier round.  The
+// caller has made the rounds' data visible (bulk-store completion and an
+// async-proxy fence).
+__device__ __forceinline__ void st_flag64_relaxed(uint64_t *p, uint64_t v)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 __device__ __forceinline__ void emit_round_single(const SignalArgs &s, int kind, int r, int b, int k)
 {
     if (s.inject == r * kNumBarriers + round_barrier(kind)) return;
-    for (int p = 0; p < s.W; ++p) st_flag64_release(round_slot(s, p, kind, b, r), s.rbase + (uint64_t)k + 1u);
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    for (int p = 0; p < s.W; ++p) st_flag64_relaxed(round_slot(s, p, kind, b, r), s.rbase + (uint64_t)k + 1u);
+}
+
+// One warp waits, on its own, for round flag k of block b of every rank
+// (lane p < W polls emitter p with acquire loads; __syncwarp then orders the
+// other lanes' later reads after them).  `avail` is the warp's count of
+// rounds every emitter is known to have published: no poll while k < avail.
+// Bounded like wait_on; on failure lane 0 records the timeout and every lane
+// returns false.
+__device__ __forceinline__ bool warp_wait_round(const SignalArgs &s, int kind, int r, int b, int k, int &avail)
+{
+    if (k < avail) return true;
+    const int lane = threadIdx.x & 31;
+    const uint64_t *slots = round_slot(s, r, kind, b, 0);
+    const uint64_t t0 = global_ns();
+    uint32_t ns = 0;
+    for (uint32_t spins = 0;; ++spins) {
+        int have = 0x7fffffff;
+        if (lane < s.W) {
+            const int64_t d = (int64_t)(ld_flag64_acquire(slots + lane) - s.rbase);
+            have = d < 0 ? 0 : (d > 0x7fffffff ? 0x7fffffff : (int)d);
+        }
+        const int mn = __reduce_min_sync(0xffffffffu, have);
+        if (mn > k) {
+            __syncwarp();
+            avail = mn;
+            return true;
+        }
+        if ((spins & 31u) == 0u) {
+            const bool bad = (lane == 0 && ld_relaxed(s.status + kStAbort) != 0u) || spins > s.max_spins ||
+                             (global_ns() - t0) > s.timeout_ns;
+            if (__any_sync(0xffffffffu, bad)) {
+                if (lane == 0) record_timeout(s, round_barrier(kind), r, b);
+                return false;
+            }
+        }
+        if (spins >= 8) {
+            __nanosleep(ns);
+            ns = ns < 224 ? ns + 32 : 256;
+        }
+    }
 }
 
 // ------------------------------------------------------------ bulk copies
