@@ -238,6 +238,8 @@ class Step:
                 events[i][1].record(self.stream)
 
     def run_e2e(self):
+        """One step end to end on one stream: every op's inputs host->device,
+        the step, every output device->host."""
         for d, h in self.e2e_pairs_in:
             d.copy_(h, non_blocking=True)
         self.run()
@@ -248,6 +250,51 @@ class Step:
         bi = sum(h.numel() * h.element_size() for _, h in self.e2e_pairs_in)
         bo = sum(h.numel() * h.element_size() for _, h in self.e2e_pairs_out)
         return bi, bo
+
+
+def run_e2e_pipelined(sets, steps, start):
+    """`steps` end-to-end steps, alternating between the Step objects in
+    `sets` (two identical sets of device and pinned host buffers, calls on
+    the same compute stream), with the host<->device copies on their own
+    streams: while step k computes and its outputs travel device->host, the
+    inputs of step k+1 travel host->device into the other set (the link is
+    full duplex).  Events keep each set's buffers safe: its inputs are
+    overwritten only after its previous step has read them, and its outputs
+    only after they have been copied out.  Every step copies all its inputs
+    in and all its outputs out.  Returns the event recorded on the compute
+    stream after the last copy out."""
+    compute = sets[0].stream
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+    cin.wait_event(start)
+    done_compute = [None] * len(sets)
+    done_out = [None] * len(sets)
+    last = None
+    for k in range(steps):
+        i = k % len(sets)
+        st = sets[i]
+        if done_compute[i] is not None:
+            cin.wait_event(done_compute[i])
+        with torch.cuda.stream(cin):
+            for d, h in st.e2e_pairs_in:
+                d.copy_(h, non_blocking=True)
+        arrived = torch.cuda.Event()
+        arrived.record(cin)
+        compute.wait_event(arrived)
+        if done_out[i] is not None:
+            compute.wait_event(done_out[i])
+        st.run()
+        done_compute[i] = torch.cuda.Event()
+        done_compute[i].record(compute)
+        cout.wait_event(done_compute[i])
+        with torch.cuda.stream(cout):
+            for d, h in st.e2e_pairs_out:
+                h.copy_(d, non_blocking=True)
+        done_out[i] = last = torch.cuda.Event()
+        last.record(cout)
+    compute.wait_event(last)
+    end = torch.cuda.Event(enable_timing=True)
+    end.record(compute)
+    return end
 
 
 def latency_sweep(rr, stream, reps=1000, batch=250):
@@ -335,6 +382,50 @@ def graph_latency(rr, stream, batch=250, reps=3):
     pad.status(stream)
     pad.close()
     return res
+
+
+def ag_sweep(rr, stream):
+    """Rank-major allgather, W=8, bf16, 1 KiB .. 512 MiB per rank (powers of
+    two), rank 0's output: GPU time per call, back to back.  Small sizes
+    rotate through several buffer sets (up to 64) so that consecutive calls
+    touch different memory; a size whose rotated sets span less than twice
+    the L2 is marked l2_resident (its GB/s is not an HBM figure)."""
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    pad = rr.rr_signal_pad_create(W)
+    sh = stream.cuda_stream
+    out = {}
+    for nbytes in workloads.AG_SWEEP["bytes_per_rank"]:
+        n = nbytes // EB
+        foot = 2 * W * nbytes
+        sets = max(1, min(64, -(-4 * l2 // foot)))
+        bufs = [(torch.empty((W, n), dtype=torch.bfloat16, device="cuda"),
+                 torch.empty(W * n, dtype=torch.bfloat16, device="cuda")) for _ in range(sets)]
+        calls = [rr.bound_call("rr_allgather", [x[r].data_ptr() for r in range(W)],
+                               [y.data_ptr()] + [None] * (W - 1), W, n, rr.RR_BF16, pad, sh)
+                 for x, y in bufs]
+        count = 400 if nbytes <= (1 << 20) else (60 if nbytes <= (64 << 20) else 10)
+        count = max(count, sets)
+        for c in calls:
+            c()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(20_000_000)
+            e0.record(stream)
+            for i in range(count):
+                calls[i % sets]()
+            e1.record(stream)
+        e1.synchronize()
+        us = 1000.0 * e0.elapsed_time(e1) / count
+        gbs = 2 * W * nbytes / us / 1e3
+        out[str(nbytes)] = {"us": round(us, 2), "GBps": round(gbs, 1),
+                            "pct_of_8TBps": round(100 * gbs / NOMINAL_HBM_GBS, 2),
+                            "l2_resident": sets * foot < 2 * l2}
+        del calls, bufs
+    pad.status(stream)
+    pad.close()
+    torch.cuda.empty_cache()
+    return out
 
 
 def fsdp_28_layers(rr, stream):
@@ -520,7 +611,7 @@ def run_gpu(args, rank, world, local_rank):
     max_ms = max_over_ranks(elapsed_ms, world)
 
     # end to end through the public API: host inputs in, host outputs out
-    e2e_steps = max(1, min(args.steps, 5))
+    e2e_steps = max(2, min(args.steps, 6))
     with torch.cuda.stream(stream):
         step.run_e2e()
     torch.cuda.synchronize()
@@ -533,7 +624,24 @@ def run_gpu(args, rank, world, local_rank):
             step.run_e2e()
         e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    e2e_serial_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    # the same steps with the copies pipelined across steps over two buffer
+    # sets (the headline e2e)
+    step_b = Step(rr, stream, seed=workloads.LARGE["seed_base"] + 97 * rank + 1, ops=ops,
+                  n=args.numel or N, pc_div=args.pc_div)
+    for opt in ("reduce_engine", "twoshot_mode"):
+        step_b.pad.set_option(opt, step.pad.get_option(opt))
+    e2e_steps_p = 2 * e2e_steps
+    with torch.cuda.stream(stream):
+        run_e2e_pipelined([step, step_b], 2, torch.cuda.Event())
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    e1 = run_e2e_pipelined([step, step_b], e2e_steps_p, e0)
+    torch.cuda.synchronize()
+    step_b.pad.status(stream)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps_p, world)
     bi, bo = step.e2e_bytes()
 
     if rank != 0:
@@ -557,6 +665,7 @@ def run_gpu(args, rank, world, local_rank):
     if not args.no_extras:
         extras["latency_us"] = latency_sweep(rr, stream)
         extras["fsdp_28_layers"] = fsdp_28_layers(rr, stream)
+        extras["allgather_sweep"] = ag_sweep(rr, stream)
         extras["overlap_gemm"] = overlap_gemm(rr, stream)
 
     line = {
@@ -586,7 +695,14 @@ def run_gpu(args, rank, world, local_rank):
         "ops_note": f"per-op breakdown from {n_prof} extra steps with an event pair around every op "
                     "(each pair adds a few us to its op); value uses the timed steps",
         "e2e": {"value": round(world * step_bytes / e2e_ms / 1e6, 1), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
+                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+                "steps": e2e_steps_p,
+                "how": "public API calls on device buffers; every step copies all inputs host->device "
+                       "from pinned memory and all outputs device->host; consecutive steps alternate "
+                       "between two buffer sets so that one step's copies in overlap the previous "
+                       "step's copies out (two copy streams)",
+                "serial_ms_per_step": round(e2e_serial_ms, 3),
+                "serial_value": round(world * step_bytes / e2e_serial_ms / 1e6, 1)},
         "gpu_launches": len(ops) * args.steps,
         "clocks": clocks,
         "cpu_baseline": None,
@@ -690,7 +806,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("rr", "reference"), default="rr")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the latency sweep, the 28-layer run and the GEMM-overlap run")
+                    help="skip the latency sweep, the 28-layer run, the allgather size sweep and the "
+                         "GEMM-overlap run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="", help="comma-separated subset of ops (profiling runs)")
     ap.add_argument("--numel", type=int, default=0, help="elements per rank for the allreduce/allgather ops")
