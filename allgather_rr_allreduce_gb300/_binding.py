@@ -27,7 +27,8 @@ RR_MAX_WORLD, RR_MAX_SPLITS = 16, 256
 
 OPTIONS = {
     "timeout_ns": 0, "blocks_per_rank": 1, "gather_engine": 2, "inject_skip": 3, "round_bytes": 4,
-    "reduce_engine": 5, "twoshot_mode": 6, "device_generation": 7,
+    "reduce_engine": 5, "twoshot_mode": 6, "device_generation": 7, "debug_iterations": 8,
+    "debug_skew_ns": 9,
     "generation": 16, "last_grid": 17, "last_blocks_per_rank": 18, "last_engine": 19,
     "world_size": 20, "max_blocks_per_rank": 21,
 }

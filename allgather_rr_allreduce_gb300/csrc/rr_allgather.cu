@@ -273,6 +273,32 @@ __global__ void __launch_bounds__(kTmaThreads) gather_kernel_tma(const __grid_co
     end_call(sig);
 }
 
+// In-launch iterations (test mode): the bodies above run a.iters times in one
+// launch (run_iterations).
+template <class Args>
+__global__ void __launch_bounds__(kLdstThreads) gather_iter_kernel_ldst(const __grid_constant__ Args a)
+{
+    run_iterations(a, begin_call(a.sig),
+                   [](const Args &ai, const SignalArgs &si) { gather_kernel_ldst_body(ai, si); });
+}
+template <class Args>
+__global__ void __launch_bounds__(kTmaThreads) gather_iter_kernel_tma(const __grid_constant__ Args a)
+{
+    run_iterations(a, begin_call(a.sig),
+                   [](const Args &ai, const SignalArgs &si) { gather_kernel_tma_body(ai, si); });
+}
+
+KernelChoice iter_gather_kernel_for(int engine, bool list)
+{
+    if (engine == 2)
+        return KernelChoice{list ? (const void *)gather_iter_kernel_tma<GatherListArgs>
+                                 : (const void *)gather_iter_kernel_tma<GatherArgs>,
+                            kTmaThreads, kTmaSmem};
+    return KernelChoice{list ? (const void *)gather_iter_kernel_ldst<GatherListArgs>
+                             : (const void *)gather_iter_kernel_ldst<GatherArgs>,
+                        kLdstThreads, 0};
+}
+
 KernelChoice gather_kernel_for(int engine, bool list)
 {
     if (engine == 2)

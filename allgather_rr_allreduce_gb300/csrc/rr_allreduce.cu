@@ -796,6 +796,62 @@ __global__ void __launch_bounds__(kSwThreads, 1) staged_kernel(const __grid_cons
     end_call(sig);
 }
 
+// ------------------------------------------- in-launch iterations (test mode)
+// The default kernels' bodies run a.iters times in one launch (see
+// run_iterations); separate instantiations, so the kernels above are
+// unchanged.  bf16 only.
+template <int WMAX>
+__global__ void __launch_bounds__(kReduceThreads, 2) oneshot_iter_kernel(const __grid_constant__ ReduceArgs a)
+{
+    run_iterations(a, begin_call(a.sig), [](const ReduceArgs &ai, const SignalArgs &si) {
+        oneshot_kernel_body<OpBF16, WMAX, false>(ai, si);
+    });
+}
+template <int WMAX>
+__global__ void __launch_bounds__(kReduceThreads, 2) twoshot_iter_kernel(const __grid_constant__ ReduceArgs a)
+{
+    run_iterations(a, begin_call(a.sig), [](const ReduceArgs &ai, const SignalArgs &si) {
+        twoshot_kernel_body<OpBF16, WMAX, false, true>(ai, si);
+    });
+}
+template <int WMAX, bool kTwoShot>
+__global__ void __launch_bounds__(kSwThreads, 1) staged_iter_kernel(const __grid_constant__ ReduceArgs a)
+{
+    run_iterations(a, begin_call(a.sig), [](const ReduceArgs &ai, const SignalArgs &si) {
+        staged_kernel_body<OpBF16, WMAX, kTwoShot>(ai, si);
+    });
+}
+
+KernelChoice iter_reduce_kernel_for(bool twoshot, int W, bool copy_mode)
+{
+    const int w = W <= 2 ? 2 : W <= 4 ? 4 : W <= 8 ? 8 : 16;
+    if (copy_mode) {
+        const void *fn = twoshot ? (w == 2 ? (const void *)staged_iter_kernel<2, true>
+                                    : w == 4 ? (const void *)staged_iter_kernel<4, true>
+                                    : w == 8 ? (const void *)staged_iter_kernel<8, true>
+                                             : (const void *)staged_iter_kernel<16, true>)
+                                 : (w == 2 ? (const void *)staged_iter_kernel<2, false>
+                                    : w == 4 ? (const void *)staged_iter_kernel<4, false>
+                                    : w == 8 ? (const void *)staged_iter_kernel<8, false>
+                                             : (const void *)staged_iter_kernel<16, false>);
+        return KernelChoice{fn, kSwThreads, kSwSmem};
+    }
+    if (twoshot) {
+        const void *fn = w == 2 ? (const void *)twoshot_iter_kernel<2>
+                         : w == 4 ? (const void *)twoshot_iter_kernel<4>
+                         : w == 8 ? (const void *)twoshot_iter_kernel<8>
+                                  : (const void *)twoshot_iter_kernel<16>;
+        KernelChoice k{fn, kReduceThreads, 0};
+        k.per_sm = 1;  // as the push two-shot without staging
+        return k;
+    }
+    const void *fn = w == 2 ? (const void *)oneshot_iter_kernel<2>
+                     : w == 4 ? (const void *)oneshot_iter_kernel<4>
+                     : w == 8 ? (const void *)oneshot_iter_kernel<8>
+                              : (const void *)oneshot_iter_kernel<16>;
+    return KernelChoice{fn, kReduceThreads, 0};
+}
+
 // ------------------------------------------------------------------ dispatch
 template <class Op, bool kCopy>
 static const void *pick_oneshot(int W)

@@ -24,6 +24,7 @@ struct rr_signal_pad {
     uint32_t *status;  // device, rr::kStatusWords words
     uint64_t *dev_gen; // device generation counter (device-generation mode)
     uint32_t *done;    // device tally of finished blocks (device-generation mode)
+    uint64_t *lflags;  // device, rank-local boundary flags (in-launch iteration mode)
     int device_gen;    // 0: host counter passed per call; 1: device counter (graph-capturable)
     uint32_t gen;      // generation of the last call (0 = none yet): low 32 bits of gen64
     uint64_t gen64;    // 64-bit call counter; round flags grow with it
@@ -33,6 +34,8 @@ struct rr_signal_pad {
     int engine;        // gathers: 0 auto, 1 ldst, 2 tma, 3 copy engines
     int reduce_engine; // one-shot with copy_mode off: 0 auto, 1 ldst, 2 tma
     int twoshot_mode;  // 0 auto, 1 pull (middle barrier), 2 push (owner broadcasts)
+    int iters;         // in-launch iterations per call (test mode; 1 = off)
+    uint32_t skew_ns;  // per-rank delay step before each iteration (test mode)
     int last_grid;
     int last_B;
     int last_engine;
@@ -169,10 +172,15 @@ int64_t round_vectors(int64_t option_bytes, int64_t pref, int64_t longest_chunk)
     return p < rr::kGranuleVec ? rr::kGranuleVec : p;
 }
 
-rr::SignalArgs signal_args(rr_signal_pad *pad)
+// Signal arguments of the next call.  A call of `iters` in-launch
+// iterations takes generations gen64 .. gen64 + iters - 1, none of whose low
+// 32-bit words may be 0 (the pad starts zeroed); consecutive generations
+// alternate in parity, across calls too.
+rr::SignalArgs signal_args(rr_signal_pad *pad, int iters = 1)
 {
     rr::SignalArgs s;
     s.flags = pad->flags;
+    s.lflags = pad->lflags;
     s.status = pad->status;
     s.timeout_ns = pad->timeout_ns;
     const uint64_t spins = pad->timeout_ns / 64 + 4096;
@@ -182,6 +190,7 @@ rr::SignalArgs signal_args(rr_signal_pad *pad)
         rr::SignalArgs d;
         std::memset(&d, 0, sizeof d);
         d.flags = pad->flags;
+        d.lflags = pad->lflags;
         d.rflags = pad->rflags;
         d.status = pad->status;
         d.timeout_ns = pad->timeout_ns;
@@ -194,11 +203,17 @@ rr::SignalArgs signal_args(rr_signal_pad *pad)
         return d;
     }
     pad->gen64 += 1;
-    if ((uint32_t)pad->gen64 == 0) pad->gen64 += 2;  // g is never 0 (the pad starts zeroed); keep the parity
-    pad->gen = (uint32_t)pad->gen64;
-    s.g = pad->gen;
+    // g is never 0 (the pad starts zeroed); skipping by 2 keeps the parity
+    auto bad = [&](uint64_t g) {
+        const uint32_t lo = (uint32_t)g;
+        return lo == 0u || (uint64_t)lo + (uint64_t)(iters - 1) > 0xffffffffull;
+    };
+    while (bad(pad->gen64)) pad->gen64 += 2;
+    s.g = (uint32_t)pad->gen64;
     s.rflags = pad->rflags;
     s.rbase = pad->gen64 << rr::kRoundBits;
+    pad->gen64 += (uint64_t)(iters - 1);
+    pad->gen = (uint32_t)pad->gen64;
     s.dev_gen = nullptr;
     s.done = nullptr;
     s.W = pad->W;
@@ -247,6 +262,18 @@ rr_status check_device(rr_signal_pad *pad)
     return RR_OK;
 }
 
+// In-launch iterations (test mode): iteration k's slices start k * stride
+// bytes after the given pointers, stride = the per-iteration size rounded up
+// to 16 bytes (every slice stays 16-byte aligned).
+int64_t iter_stride(int64_t bytes) { return (bytes + 15) & ~(int64_t)15; }
+bool iterating(const rr_signal_pad *pad) { return pad->iters > 1 || pad->skew_ns > 0; }
+rr_status check_iterating(const rr_signal_pad *pad)
+{
+    if (pad->device_gen)
+        return fail(RR_ERR_INVALID_ARG, "in-launch iterations need the host generation counter (device_generation 0)");
+    return RR_OK;
+}
+
 rr_status allreduce_common(bool twoshot, const void *const *inputs, void *const *rank_bufs,
                            void *const *outputs, int W, int64_t numel, rr_dtype dtype, int copy_mode,
                            rr_signal_pad *pad, cudaStream_t stream)
@@ -259,6 +286,21 @@ rr_status allreduce_common(bool twoshot, const void *const *inputs, void *const 
     if (!rank_bufs || !outputs) return fail(RR_ERR_INVALID_ARG, "rank_bufs / outputs array is NULL");
     if (copy_mode && !inputs) return fail(RR_ERR_INVALID_ARG, "copy_mode needs the inputs array");
     const int64_t bytes = numel * eb;
+    const bool iterate = iterating(pad);
+    if (iterate) {
+        st = check_iterating(pad);
+        if (st != RR_OK) return st;
+        if (dtype != RR_BF16) return fail(RR_ERR_INVALID_ARG, "in-launch iterations run bf16 reductions only");
+        if (twoshot && pad->twoshot_mode == 1)
+            return fail(RR_ERR_INVALID_ARG, "in-launch iterations run the push two-shot only");
+        if (pad->reduce_engine != 0)
+            return fail(RR_ERR_INVALID_ARG, "in-launch iterations run the automatic reduce engine only");
+    }
+    // bytes each pointer covers: every iteration's slice (rank buffers too
+    // with copy_mode off; with copy_mode on every iteration stages into the
+    // same rank buffers)
+    const int64_t span_io = iterate ? iter_stride(bytes) * (pad->iters - 1) + bytes : bytes;
+    const int64_t span_buf = copy_mode ? bytes : span_io;
     int nout = 0;
     for (int r = 0; r < W; ++r) {
         if (!rank_bufs[r]) return fail(RR_ERR_INVALID_ARG, "rank_bufs[%d] is NULL", r);
@@ -279,23 +321,23 @@ rr_status allreduce_common(bool twoshot, const void *const *inputs, void *const 
     // rank_bufs[r] (the sum replaces every rank's buffer).
     const bool in_place_ok = twoshot && !copy_mode;
     for (int i = 0; i < W; ++i) {
-        const Span bi = span_of(rank_bufs[i], bytes);
+        const Span bi = span_of(rank_bufs[i], span_buf);
         for (int j = 0; j < W; ++j) {
-            if (j > i && overlaps(bi, span_of(rank_bufs[j], bytes)))
+            if (j > i && overlaps(bi, span_of(rank_bufs[j], span_buf)))
                 return fail(RR_ERR_ALIAS, "rank_bufs[%d] and rank_bufs[%d] overlap", i, j);
-            if (copy_mode && overlaps(bi, span_of(inputs[j], bytes)))
+            if (copy_mode && overlaps(bi, span_of(inputs[j], span_io)))
                 return fail(RR_ERR_ALIAS, "rank_bufs[%d] and inputs[%d] overlap", i, j);
             if (in_place_ok && i == j && outputs[j] == rank_bufs[i]) continue;
-            if (outputs[j] && overlaps(bi, span_of(outputs[j], bytes)))
+            if (outputs[j] && overlaps(bi, span_of(outputs[j], span_io)))
                 return fail(RR_ERR_ALIAS, "rank_bufs[%d] and outputs[%d] overlap%s", i, j,
                             i == j && !in_place_ok ? " (only the two-shot with copy_mode off runs in place)" : "");
         }
         if (!outputs[i]) continue;
-        const Span oi = span_of(outputs[i], bytes);
+        const Span oi = span_of(outputs[i], span_io);
         for (int j = 0; j < W; ++j) {
-            if (j > i && outputs[j] && overlaps(oi, span_of(outputs[j], bytes)))
+            if (j > i && outputs[j] && overlaps(oi, span_of(outputs[j], span_io)))
                 return fail(RR_ERR_ALIAS, "outputs[%d] and outputs[%d] overlap", i, j);
-            if (copy_mode && overlaps(oi, span_of(inputs[j], bytes)))
+            if (copy_mode && overlaps(oi, span_of(inputs[j], span_io)))
                 return fail(RR_ERR_ALIAS, "outputs[%d] and inputs[%d] overlap", i, j);
         }
     }
@@ -310,8 +352,9 @@ rr_status allreduce_common(bool twoshot, const void *const *inputs, void *const 
     // one-shot, 172 vs 175 us two-shot at W=8 x 32 MiB), loads/stores otherwise
     const bool tma = copy_mode ? (pad->reduce_engine != 1 && (!twoshot || push))
                                : (!twoshot && pad->reduce_engine == 2);
-    const rr::KernelChoice k = tma ? (copy_mode ? rr::staged_kernel_for(dtype, W, twoshot)
-                                                : rr::oneshot_tma_kernel_for(dtype, W))
+    const rr::KernelChoice k = iterate ? rr::iter_reduce_kernel_for(twoshot, W, copy_mode != 0)
+                               : tma ? (copy_mode ? rr::staged_kernel_for(dtype, W, twoshot)
+                                                  : rr::oneshot_tma_kernel_for(dtype, W))
                                : twoshot ? rr::twoshot_kernel_for(dtype, W, copy_mode != 0, push)
                                          : rr::oneshot_kernel_for(dtype, W, copy_mode != 0);
     int64_t moved = twoshot ? bytes * (W + 1) + (int64_t)(W - 1) * bytes * 2
@@ -345,10 +388,20 @@ rr_status allreduce_common(bool twoshot, const void *const *inputs, void *const 
         const int64_t pref = twoshot ? ((tma && copy_mode) ? 2048 : 512) : ((tma && copy_mode) ? 16384 : 4096);
         a.round_vec = round_vectors(pad->round_bytes, pref, longest);
     }
-    a.sig = signal_args(pad);
+    a.iters = iterate ? pad->iters : 1;
+    a.skew_ns = iterate ? pad->skew_ns : 0u;
+    a.stride = iter_stride(bytes);
+    a.sig = signal_args(pad, a.iters);
     pad->last_B = B;
     pad->last_engine = tma ? 2 : 1;
     return launch(pad, k, W * B, a, stream);
+}
+
+// Bytes a gather pointer covers: `bytes` per call, or every iteration's
+// slice in the in-launch iteration mode.
+int64_t gather_span(const rr_signal_pad *pad, int64_t bytes)
+{
+    return iterating(pad) ? iter_stride(bytes) * (pad->iters - 1) + bytes : bytes;
 }
 
 // Checks shared by every gather: pad, dtype, split table (-> a.off, in
@@ -394,6 +447,12 @@ rr_status run_gather(rr_signal_pad *pad, Args &a, int64_t shard, bool list, cuda
     rr_status st = check_device(pad);
     if (st != RR_OK) return st;
     const int engine = pad->engine == 0 ? 2 : pad->engine;
+    const bool iterate = iterating(pad);
+    if (iterate) {
+        st = check_iterating(pad);
+        if (st != RR_OK) return st;
+        if (engine == 3) return fail(RR_ERR_INVALID_ARG, "in-launch iterations run the gather kernels, not the copy engines");
+    }
     if (engine == 3) {
         for (int q = 0; q < a.nout; ++q)
             for (int r = 0; r < a.W; ++r)
@@ -410,12 +469,16 @@ rr_status run_gather(rr_signal_pad *pad, Args &a, int64_t shard, bool list, cuda
         pad->last_engine = 3;
         return ok();
     }
-    const rr::KernelChoice k = rr::gather_kernel_for(engine, list);
+    const rr::KernelChoice k = iterate ? rr::iter_gather_kernel_for(engine, list) : rr::gather_kernel_for(engine, list);
     int B = 0;
     st = plan_blocks(pad, k, a.W, shard * a.W + shard * a.W * a.nout, &B);
     if (st != RR_OK) return st;
     a.B = B;
-    a.sig = signal_args(pad);
+    a.iters = iterate ? pad->iters : 1;
+    a.skew_ns = iterate ? pad->skew_ns : 0u;
+    a.src_stride = iter_stride(shard);
+    a.out_stride = iter_stride(shard * a.W);
+    a.sig = signal_args(pad, a.iters);
     pad->last_B = B;
     pad->last_engine = engine;
     return launch(pad, k, a.W * B, a, stream);
@@ -440,13 +503,14 @@ rr_status gather_common(const void *const *rank_bufs, void *const *outputs, int 
         }
     }
     if (a.nout == 0) return fail(RR_ERR_INVALID_ARG, "no output is materialised");
+    const int64_t ospan = gather_span(pad, outb), sspan = gather_span(pad, shard);
     for (int i = 0; i < W; ++i) {
         if (!outputs[i]) continue;
-        const Span oi = span_of(outputs[i], outb);
+        const Span oi = span_of(outputs[i], ospan);
         for (int j = 0; j < W; ++j) {
-            if (j > i && outputs[j] && overlaps(oi, span_of(outputs[j], outb)))
+            if (j > i && outputs[j] && overlaps(oi, span_of(outputs[j], ospan)))
                 return fail(RR_ERR_ALIAS, "outputs[%d] and outputs[%d] overlap", i, j);
-            if (overlaps(oi, span_of(rank_bufs[j], shard)))
+            if (overlaps(oi, span_of(rank_bufs[j], sspan)))
                 return fail(RR_ERR_ALIAS, "outputs[%d] and rank_bufs[%d] overlap", i, j);
         }
     }
@@ -479,15 +543,16 @@ rr_status gather_list_impl(const void *const *rank_bufs, void *const *out_lists,
     }
     if (a.nout == 0) return fail(RR_ERR_INVALID_ARG, "no output is materialised");
     // Every list buffer against every other one and every rank buffer.
+    const int64_t sspan = gather_span(pad, shard);
     for (int i = 0; i < W * W; ++i) {
         if (!a.lst[i]) continue;
-        const Span si = span_of(a.lst[i], shard);
+        const Span si = span_of(a.lst[i], sspan);
         for (int j = i + 1; j < W * W; ++j)
-            if (a.lst[j] && overlaps(si, span_of(a.lst[j], shard)))
+            if (a.lst[j] && overlaps(si, span_of(a.lst[j], sspan)))
                 return fail(RR_ERR_ALIAS, "output list %d entry %d and list %d entry %d overlap", i / W, i % W,
                             j / W, j % W);
         for (int r = 0; r < W; ++r)
-            if (overlaps(si, span_of(rank_bufs[r], shard)))
+            if (overlaps(si, span_of(rank_bufs[r], sspan)))
                 return fail(RR_ERR_ALIAS, "output list %d entry %d and rank_bufs[%d] overlap", i / W, i % W, r);
     }
     if (shard == 0) return ok();
@@ -516,7 +581,10 @@ rr_status rr_signal_pad_create(int world_size, int max_blocks_per_rank, uint64_t
     const size_t flag_bytes = ((nflags * sizeof(uint32_t) + 255) / 256) * 256;
     const size_t rflag_bytes = nrflags * sizeof(uint64_t);
     const size_t status_bytes = rr::kStatusWords * sizeof(uint32_t);  // 32: keeps 8-byte alignment
-    const size_t bytes = flag_bytes + rflag_bytes + status_bytes + sizeof(uint64_t) + sizeof(uint32_t);
+    // after the generation counter and the block tally: the rank-local
+    // boundary flags of the in-launch iteration mode, [W][Bmax] uint64
+    const size_t lflag_off = ((flag_bytes + rflag_bytes + status_bytes + sizeof(uint64_t) + sizeof(uint32_t) + 7) / 8) * 8;
+    const size_t bytes = lflag_off + (size_t)world_size * Bmax * sizeof(uint64_t);
     void *mem = nullptr;
     e = cudaMalloc(&mem, bytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(signal pad)");
@@ -537,7 +605,9 @@ rr_status rr_signal_pad_create(int world_size, int max_blocks_per_rank, uint64_t
     p->status = reinterpret_cast<uint32_t *>(static_cast<char *>(mem) + flag_bytes + rflag_bytes);
     p->dev_gen = reinterpret_cast<uint64_t *>(static_cast<char *>(mem) + flag_bytes + rflag_bytes + status_bytes);
     p->done = reinterpret_cast<uint32_t *>(p->dev_gen + 1);
+    p->lflags = reinterpret_cast<uint64_t *>(static_cast<char *>(mem) + lflag_off);
     p->inject = -1;
+    p->iters = 1;
     *out = p;
     return ok();
 }
@@ -625,6 +695,14 @@ rr_status rr_signal_pad_set_option(rr_signal_pad *pad, rr_option opt, int64_t va
         if (value < 0 || value > 2) return fail(RR_ERR_INVALID_ARG, "two-shot mode %lld", (long long)value);
         pad->twoshot_mode = (int)value;
         return ok();
+    case RR_OPT_DEBUG_ITERATIONS:
+        if (value < 1 || value > 4096) return fail(RR_ERR_INVALID_ARG, "iterations %lld outside 1..4096", (long long)value);
+        pad->iters = (int)value;
+        return ok();
+    case RR_OPT_DEBUG_SKEW_NS:
+        if (value < 0 || value > 1000000) return fail(RR_ERR_INVALID_ARG, "skew %lld ns outside 0..1e6", (long long)value);
+        pad->skew_ns = (uint32_t)value;
+        return ok();
     case RR_OPT_DEVICE_GENERATION: {
         if (value < 0 || value > 1) return fail(RR_ERR_INVALID_ARG, "device generation %lld", (long long)value);
         if ((int)value == pad->device_gen) return ok();
@@ -673,6 +751,8 @@ rr_status rr_signal_pad_get_option(rr_signal_pad *pad, rr_option opt, int64_t *v
         }
         break;
     case RR_OPT_DEVICE_GENERATION: *value = pad->device_gen; break;
+    case RR_OPT_DEBUG_ITERATIONS: *value = pad->iters; break;
+    case RR_OPT_DEBUG_SKEW_NS: *value = pad->skew_ns; break;
     case RR_OPT_LAST_GRID: *value = pad->last_grid; break;
     case RR_OPT_LAST_BLOCKS_PER_RANK: *value = pad->last_B; break;
     case RR_OPT_LAST_ENGINE: *value = pad->last_engine; break;

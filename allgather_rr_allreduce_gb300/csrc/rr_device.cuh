@@ -387,6 +387,118 @@ __device__ __forceinline__ void end_call(const SignalArgs &s)
     }
 }
 
+// ------------------------------------------- in-launch iterations (test mode)
+// Several calls in one launch, so that the barriers between one call's end and
+// the next call's start are crossed without a kernel boundary in between (on
+// several GPUs there is none): iteration k runs with generation g + k and the
+// round base of call gen64 + k (the host reserves that range), on its own
+// slices of the inputs and outputs.
+
+// Rank r's blocks sleep ((r + k) mod W) * skew_ns before iteration k, so that
+// the ranks reach each barrier out of step.
+__device__ __forceinline__ void skew_delay(const SignalArgs &s, int r, int k, uint32_t skew_ns)
+{
+    if (skew_ns == 0u) return;
+    const uint64_t d = (uint64_t)((r + k) % s.W) * skew_ns;
+    const uint64_t t0 = global_ns();
+    while (global_ns() - t0 < d) __nanosleep(1000);
+}
+__device__ __forceinline__ SignalArgs iteration_signal(const SignalArgs &s, int k)
+{
+    SignalArgs t = s;
+    t.g = s.g + (uint32_t)k;
+    t.rbase = s.rbase + ((uint64_t)k << kRoundBits);
+    return t;
+}
+__device__ __forceinline__ void advance_args(ReduceArgs &ai, const ReduceArgs &a, int k)
+{
+    const int64_t off = (int64_t)k * a.stride;
+    for (int r = 0; r < a.W; ++r) {
+        if (a.in[r]) ai.in[r] = static_cast<const char *>(a.in[r]) + off;
+        if (!a.copy_mode) ai.buf[r] = static_cast<char *>(a.buf[r]) + off;
+        if (a.out[r]) ai.out[r] = static_cast<char *>(a.out[r]) + off;
+    }
+}
+__device__ __forceinline__ void advance_args(GatherArgs &ai, const GatherArgs &a, int k)
+{
+    for (int r = 0; r < a.W; ++r) {
+        ai.src[r] = static_cast<const char *>(a.src[r]) + (int64_t)k * a.src_stride;
+        if (a.out[r]) ai.out[r] = static_cast<char *>(a.out[r]) + (int64_t)k * a.out_stride;
+    }
+}
+__device__ __forceinline__ void advance_args(GatherListArgs &ai, const GatherListArgs &a, int k)
+{
+    for (int r = 0; r < a.W; ++r) ai.src[r] = static_cast<const char *>(a.src[r]) + (int64_t)k * a.src_stride;
+    for (int i = 0; i < a.W * a.W; ++i)
+        if (a.lst[i]) ai.lst[i] = static_cast<char *>(a.lst[i]) + (int64_t)k * a.src_stride;
+}
+
+// The boundary between two iterations of one rank: every block of rank r
+// has finished iteration k before any starts iteration k + 1, as the kernel
+// boundary between two calls on one GPU guarantees.  Without it, block 0 of
+// a rank (the only emitter of its ARRIVE flag) could run two calls ahead of
+// another block of the same rank and overwrite, in the same parity half,
+// the flag that block is still waiting for.  The ranks stay free to drift
+// against each other: only the collective's own barriers order them.  Block
+// b of rank r stores rbase_k + 1 into its slot (values only grow) and waits,
+// bounded, until every block of rank r has stored at least that.
+__device__ __forceinline__ bool rank_boundary(const SignalArgs &s, int r, int b, int B, int *s_ok)
+{
+    __syncthreads();
+    uint64_t *slots = s.lflags + (size_t)r * s.Bmax;
+    const uint64_t target = s.rbase + 1u;
+    if (threadIdx.x == 0) st_flag64_release(slots + b, target);
+    if (threadIdx.x < 32) {
+        // warp 0 polls the B slots of rank r (lane i: slots i, i + 32, ...)
+        const uint64_t t0 = global_ns();
+        bool ok = true;
+        for (uint32_t spins = 0;; ++spins) {
+            bool seen = true;
+            for (int j = threadIdx.x; j < B; j += 32)
+                if ((int64_t)(ld_flag64_acquire(slots + j) - target) < 0) seen = false;
+            if (__all_sync(0xffffffffu, seen)) break;
+            if ((spins & 31u) == 0u) {
+                const bool bad = (threadIdx.x == 0 && ld_relaxed(s.status + kStAbort) != 0u) ||
+                                 spins > s.max_spins || (global_ns() - t0) > s.timeout_ns;
+                if (__any_sync(0xffffffffu, bad)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (spins >= 8) __nanosleep(128);
+        }
+        if (!ok && threadIdx.x == 0) record_timeout(s, RR_BARRIER_END, r, b);
+        if (threadIdx.x == 0) *s_ok = ok ? 1 : 0;
+    }
+    __syncthreads();
+    return *s_ok != 0;
+}
+
+// Run body(args of iteration k, signal of iteration k) for k = 0..iters-1,
+// with a rank-local boundary between iterations; stop once any wait of the
+// call has given up (the pad's abort word, read by one thread and shared
+// with the block).
+template <class Args, class Body>
+__device__ __forceinline__ void run_iterations(const Args &a, const SignalArgs &sig, Body body)
+{
+    __shared__ int s_stop;
+    Args ai = a;
+    const int r = blockIdx.x / a.B;
+    const int b = blockIdx.x - r * a.B;
+    for (int k = 0; k < a.iters; ++k) {
+        if (k > 0) {
+            if (!rank_boundary(iteration_signal(sig, k - 1), r, b, a.B, &s_stop)) return;
+            __syncthreads();
+            if (threadIdx.x == 0) s_stop = ld_relaxed(sig.status + kStAbort) != 0u;
+            __syncthreads();
+            if (s_stop) return;
+            advance_args(ai, a, k);
+        }
+        skew_delay(sig, r, k, a.skew_ns);
+        body(ai, iteration_signal(sig, k));
+    }
+}
+
 // ---------------------------------------------------------------- arithmetic
 // A 16-byte vector holds kEPV elements.  combine() adds the W vectors
 // x[0..W-1] element-wise: binary32 accumulator starting at rank 0's value,

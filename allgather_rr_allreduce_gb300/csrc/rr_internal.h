@@ -50,6 +50,9 @@ struct SignalArgs {
     // (counted in *done) advances it.
     uint64_t *dev_gen;
     uint32_t *done;
+    // In-launch iteration mode: [W][Bmax] flags through which the blocks of
+    // one rank meet between iterations (null when the pad has none).
+    uint64_t *lflags;
 };
 
 // One-shot and two-shot allreduce.
@@ -66,6 +69,13 @@ struct ReduceArgs {
     int nout;                      // number of materialised outputs
     int qlist[RR_MAX_WORLD];       // their ranks, ascending
     SignalArgs sig;
+    // In-launch iterations (test mode): iteration k works on inputs and
+    // outputs (and, with copy_mode off, rank buffers) advanced by k * stride
+    // bytes; with copy_mode on every iteration stages into the same rank
+    // buffers.  Rank r's blocks sleep ((r + k) mod W) * skew_ns first.
+    int iters;
+    uint32_t skew_ns;
+    int64_t stride;
 };
 
 // Rank-major and param-contiguous allgather (rank-major = one split).
@@ -79,6 +89,12 @@ struct GatherArgs {
     int nout;
     int qlist[RR_MAX_WORLD];
     SignalArgs sig;
+    // In-launch iterations (test mode): iteration k reads the shards advanced
+    // by k * src_stride bytes and writes the outputs advanced by k * out_stride.
+    int iters;
+    uint32_t skew_ns;
+    int64_t src_stride;
+    int64_t out_stride;
 };
 
 // List-output allgather (torch.distributed.all_gather): output q is W
@@ -175,5 +191,10 @@ KernelChoice oneshot_tma_kernel_for(rr_dtype dtype, int W);  // copy_mode off, b
 // copy_mode on, staging by a bulk-copy producer warp (two-shot: push allgather)
 KernelChoice staged_kernel_for(rr_dtype dtype, int W, bool twoshot);
 KernelChoice gather_kernel_for(int engine, bool list);  // 1 = loads/stores, 2 = TMA bulk
+// In-launch iteration kernels (test mode): bf16 reductions on the default
+// engines (one-shot: loads/stores, or bulk-copy staging for copy_mode; two-shot:
+// push, or bulk-copy staging for copy_mode) and both gather kernel engines.
+KernelChoice iter_reduce_kernel_for(bool twoshot, int W, bool copy_mode);
+KernelChoice iter_gather_kernel_for(int engine, bool list);
 
 }  // namespace rr

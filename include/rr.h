@@ -107,6 +107,23 @@ typedef enum {
                                    last block of each call advances, so that calls captured
                                    in a CUDA graph stay correct on every replay.  Switching
                                    synchronises the device; the pad must be idle */
+    RR_OPT_DEBUG_ITERATIONS = 8, /* test mode, default 1: each call runs n complete calls inside
+                                   one launch, iteration k with generation g + k, so the barriers
+                                   that separate one call from the next are crossed without a
+                                   kernel boundary (as on several GPUs, where there is none).
+                                   Iteration k uses the inputs, outputs and (copy_mode off) rank
+                                   buffers advanced by k * S bytes, S = the per-call size of that
+                                   pointer rounded up to 16 bytes (allgather outputs: W * shard
+                                   bytes rounded up); with copy_mode on every iteration stages
+                                   into the same rank buffers, so a rank that restaged before a
+                                   peer finished reading would corrupt that peer's result.
+                                   Every buffer must hold all n slices.  bf16 reductions on the
+                                   automatic engines (push two-shot) and the gather kernels
+                                   (not the copy engines); needs device generation off */
+    RR_OPT_DEBUG_SKEW_NS = 9,   /* test mode, default 0 (max 1e6): before iteration k every block
+                                   of rank r sleeps ((r + k) mod W) * skew ns, so the ranks reach
+                                   every barrier out of step.  Non-zero selects the test-mode
+                                   kernels even with one iteration */
     /* read-only */
     RR_OPT_GENERATION = 16,     /* generation flag value of the last call (device-generation
                                    mode: reads the device counter, synchronising the device) */
