@@ -279,3 +279,39 @@ def test_param_contiguous_unsplit_weights_qwen_layer_shapes(oracle_mod):
     full, shards = workloads.fsdp_layer_shards(W, layer=1, params=params)
     got = oracle_mod.allgather_param_contiguous(shards, workloads.shard_sizes(params, W), "bf16")
     assert np.array_equal(got, np.concatenate(full))
+
+
+def node_block_scatter(shards, splits, G):
+    """The PR's node-block form of the param-contiguous gather ("ccl:
+    hierarchical cross-node AllGather (intra-node SDMA + inter-node RDMA)
+    #441", the commit adding enqueue_param_contiguous), written out
+    independently of the oracle: ranks come in node blocks of G; for node
+    block m and param s the scatter starts at O_s*W + m*G*E_s and the ranks
+    of the block follow each other at a stride of E_s."""
+    W = len(shards)
+    S = sum(splits)
+    out = np.full(W * S, -1, dtype=np.int64)
+    for m in range(W // G):
+        o = 0
+        for e in splits:
+            block_offset = o * W + m * G * e
+            for j in range(G):
+                r = m * G + j
+                dst = block_offset + j * e
+                out[dst:dst + e] = shards[r][o:o + e]
+            o += e
+    return out
+
+
+@pytest.mark.parametrize("W", [4, 8, 6])
+def test_param_contiguous_independent_of_node_grouping(oracle_mod, W):
+    """Every node-block size G that divides W puts every byte where the
+    oracle's single formula does: G is not an argument of the layout."""
+    splits = [5, 0, 9, 1, 16]
+    S = sum(splits)
+    shards = [np.arange(r * 10_000, r * 10_000 + S, dtype=np.int32) for r in range(W)]
+    want = oracle_mod.allgather_param_contiguous(shards, splits, "int32")
+    for G in [g for g in range(1, W + 1) if W % g == 0]:
+        got = node_block_scatter(shards, splits, G)
+        assert (got >= 0).all(), f"G={G} leaves holes"
+        assert np.array_equal(got, want.astype(np.int64)), f"G={G}"
