@@ -121,3 +121,54 @@ def test_graph_replays_stay_correct(rr, algo):
             outs[i].check_guards()
     assert pad.get_option("generation") >= 1 + K * replays
     pad.close()
+
+
+@pytest.mark.parametrize("engine", [1, 2])
+def test_graph_replays_param_contiguous_and_list(rr, engine):
+    """Param-contiguous and list-output gathers captured together in one
+    graph (alternating), replayed with new shards each time."""
+    W, replays = 8, 3
+    splits = [20_000, 5, 0, 45_539]
+    S = sum(splits)
+    pad = rr.rr_signal_pad_create(W)
+    pad.set_option("device_generation", 1)
+    pad.set_option("gather_engine", engine)
+    src = RankBuffers(W, S, "bf16")
+    pc_out = [GuardedOutputs(W, W * S, "bf16", materialise=(0, 7)) for _ in range(2)]
+    lists = [[GuardedOutputs(W, S, "bf16") for _ in range(2)] for _ in range(2)]  # [call][row q in (2, 5)]
+
+    def rows(i):
+        return [lists[i][0].ptrs if q == 2 else lists[i][1].ptrs if q == 5 else None for q in range(W)]
+
+    stream = torch.cuda.Stream()
+    src.fill(workloads.rank_buffers(W, S, "bf16", "bits", seed_base=9500))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        rr.rr_allgather_param_contiguous(src.ptrs, pc_out[0].ptrs, W, splits, "bf16", pad, stream)
+        rr.rr_allgather_list(src.ptrs, rows(0), W, S, "bf16", pad, stream)
+    pad.status(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        cs = torch.cuda.current_stream()
+        for i in range(2):
+            rr.rr_allgather_param_contiguous(src.ptrs, pc_out[i].ptrs, W, splits, "bf16", pad, cs)
+            rr.rr_allgather_list(src.ptrs, rows(i), W, S, "bf16", pad, cs)
+    for j in range(replays):
+        ins = workloads.rank_buffers(W, S, "bf16", "bits", seed_base=9600 + 10 * j)
+        src.fill(ins)
+        for o in pc_out + [x for row in lists for x in row]:
+            o.poison()
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        pad.status(stream)
+        want_pc = oracle.allgather_param_contiguous(ins, splits, "bf16")
+        for i in range(2):
+            for q in (0, 7):
+                assert_bitwise(pc_out[i].host(q), want_pc, f"replay {j} call {i} param-contiguous output {q}")
+            for row in lists[i]:
+                for r in range(W):
+                    assert_bitwise(row.host(r), ins[r], f"replay {j} call {i} list entry {r}")
+                row.check_guards()
+            pc_out[i].check_guards()
+    pad.close()
