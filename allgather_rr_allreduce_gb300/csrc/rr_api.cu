@@ -107,7 +107,10 @@ rr_status resident_blocks(int dev, const rr::KernelChoice &k, int *out)
     auto key = std::make_pair(dev, k.fn);
     auto oit = g_occ.find(key);
     if (oit == g_occ.end()) {
-        if (k.smem > 48 * 1024) {
+        // The default limit covers 48 KiB of static + dynamic shared memory,
+        // so any dynamic amount is declared (a 48 KiB ring beside a few
+        // static words would otherwise fit no block at all).
+        if (k.smem > 0) {
             cudaError_t e = cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem);
             if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(maxDynamicSharedMemorySize)");
         }
