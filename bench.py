@@ -384,6 +384,30 @@ def graph_latency(rr, stream, batch=250, reps=3):
     return res
 
 
+def ops_alone(step, reps=50):
+    """Each op of the step on its own: `reps` back-to-back calls on the op's
+    buffers (inputs larger than L2) between one pair of events, so each call
+    also absorbs only its own predecessor's L2 write-back."""
+    out = {}
+    bytes_by_op = step.bytes_by_op()
+    for name in step.ops:
+        call = step.calls[name]
+        for _ in range(5):
+            call()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(step.stream)
+        for _ in range(reps):
+            call()
+        e1.record(step.stream)
+        e1.synchronize()
+        us = 1000.0 * e0.elapsed_time(e1) / reps
+        gbs = bytes_by_op[name] / us / 1e3
+        out[name] = {"us": round(us, 2), "GBps": round(gbs, 1), "pct_of_8TBps": round(100 * gbs / NOMINAL_HBM_GBS, 2)}
+    step.pad.status(step.stream)
+    return out
+
+
 def ag_sweep(rr, stream):
     """Rank-major allgather, W=8, bf16, 1 KiB .. 512 MiB per rank (powers of
     two), rank 0's output: GPU time per call, back to back.  Small sizes
@@ -663,6 +687,7 @@ def run_gpu(args, rank, world, local_rank):
 
     extras = {}
     if not args.no_extras:
+        extras["ops_alone"] = ops_alone(step)
         extras["latency_us"] = latency_sweep(rr, stream)
         extras["fsdp_28_layers"] = fsdp_28_layers(rr, stream)
         extras["allgather_sweep"] = ag_sweep(rr, stream)
@@ -806,8 +831,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("rr", "reference"), default="rr")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the latency sweep, the 28-layer run, the allgather size sweep and the "
-                         "GEMM-overlap run")
+                    help="skip the per-op standalone timing, the latency sweep, the 28-layer run, the "
+                         "allgather size sweep and the GEMM-overlap run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="", help="comma-separated subset of ops (profiling runs)")
     ap.add_argument("--numel", type=int, default=0, help="elements per rank for the allreduce/allgather ops")
