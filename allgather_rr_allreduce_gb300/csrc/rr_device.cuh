@@ -91,12 +91,6 @@ static __device__ __noinline__ void record_timeout(const SignalArgs &s, int bar,
 struct CtaSync {
     __device__ void operator()() const { __syncthreads(); }
 };
-// Named barrier 1 over the first n threads (the consumer warps of a
-// warp-specialised block, while its producer warp runs on).
-struct GroupSync {
-    int n;
-    __device__ void operator()() const { asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory"); }
-};
 
 template <class Poll, class Sync = CtaSync>
 __device__ __forceinline__ bool wait_on(const SignalArgs &s, int bar, int r, int b, Poll poll, int *s_ok,
