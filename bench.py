@@ -344,6 +344,41 @@ def latency_sweep(rr, stream, reps=1000, batch=250):
     return out
 
 
+def small_config_latency(rr, stream, reps=1000):
+    """The small workload (W=2, bf16, 4096 elements per rank, U[-1,1]):
+    one-shot allreduce and rank-major allgather into rank 0's output, GPU
+    time per call over `reps` back-to-back calls queued behind a sleep."""
+    cfg = workloads.SMALL
+    W2, n = cfg["W"], cfg["N"]
+    g = torch.Generator(device="cuda").manual_seed(cfg["seed_base"])
+    x = (torch.rand((W2, n), generator=g, device="cuda") * 2 - 1).to(torch.bfloat16)
+    y = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    z = torch.empty(W2 * n, dtype=torch.bfloat16, device="cuda")
+    pad = rr.rr_signal_pad_create(W2)
+    sh = stream.cuda_stream
+    rows = [x[r].data_ptr() for r in range(W2)]
+    calls = {"oneshot_allreduce": rr.bound_call("rr_allreduce_oneshot", None, rows, [y.data_ptr(), None], W2, n,
+                                                rr.RR_BF16, 0, pad, sh),
+             "allgather": rr.bound_call("rr_allgather", rows, [z.data_ptr(), None], W2, n, rr.RR_BF16, pad, sh)}
+    out = {"workload": cfg["name"]}
+    for name, call in calls.items():
+        for _ in range(20):
+            call()
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(20_000_000)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                call()
+            e1.record(stream)
+        e1.synchronize()
+        out[f"{name}_us"] = round(1000.0 * e0.elapsed_time(e1) / reps, 3)
+    pad.status(stream)
+    pad.close()
+    return out
+
+
 def graph_latency(rr, stream, batch=250, reps=3):
     """The same calls captured in a CUDA graph (pad with the device-resident
     generation counter), replayed back to back: GPU time per call."""
@@ -405,6 +440,40 @@ def ops_alone(step, reps=50):
         gbs = bytes_by_op[name] / us / 1e3
         out[name] = {"us": round(us, 2), "GBps": round(gbs, 1), "pct_of_8TBps": round(100 * gbs / NOMINAL_HBM_GBS, 2)}
     step.pad.status(step.stream)
+    return out
+
+
+def ag_sweep_dtypes(rr, stream, sizes=(1 << 20, 1 << 25, 1 << 29)):
+    """The rank-major allgather at a few sizes per rank for every dtype
+    (W=8, rank 0's output, 10 back-to-back calls each): the copy moves raw
+    bytes, so the dtype should not matter."""
+    pad = rr.rr_signal_pad_create(W)
+    sh = stream.cuda_stream
+    out = {}
+    for dtype in ("bf16", "fp16", "fp32", "int32"):
+        eb = workloads.ELEM_BYTES[dtype]
+        tdt = workloads.TORCH_DTYPE[dtype]
+        for nbytes in sizes:
+            n = nbytes // eb
+            x = torch.empty((W, n), dtype=tdt, device="cuda")
+            y = torch.empty(W * n, dtype=tdt, device="cuda")
+            call = rr.bound_call("rr_allgather", [x[r].data_ptr() for r in range(W)],
+                                 [y.data_ptr()] + [None] * (W - 1), W, n, rr.dtype_code(dtype), pad, sh)
+            call()
+            count = 40 if nbytes < (1 << 24) else 10
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(count):
+                call()
+            e1.record(stream)
+            e1.synchronize()
+            us = 1000.0 * e0.elapsed_time(e1) / count
+            out[f"{dtype}_{nbytes}"] = {"us": round(us, 2), "GBps": round(2 * W * nbytes / us / 1e3, 1)}
+            del x, y
+    pad.status(stream)
+    pad.close()
+    torch.cuda.empty_cache()
     return out
 
 
@@ -486,7 +555,8 @@ def fsdp_28_layers(rr, stream):
     ms = min(times)
     total = cfg["layers"] * 2 * W * S * EB
     return {"ms": round(ms, 4), "GBps": round(total / ms / 1e6, 1), "bytes": total,
-            "pct_of_8TBps": round(100 * total / ms / 1e6 / NOMINAL_HBM_GBS, 2)}
+            "pct_of_8TBps": round(100 * total / ms / 1e6 / NOMINAL_HBM_GBS, 2),
+            "us_per_layer": round(1000 * ms / cfg["layers"], 2)}
 
 
 def overlap_gemm(rr, stream, n_ag=40, mkn=8192):
@@ -676,8 +746,10 @@ def run_gpu(args, rank, world, local_rank):
     for name in ops:
         ms = statistics.mean(per_op_ms[name])
         gbs = bytes_by_op[name] / ms / 1e6
+        qs = statistics.quantiles(per_op_ms[name], n=10) if len(per_op_ms[name]) >= 10 else [ms] * 9
         op_stats[name] = {"bytes": bytes_by_op[name], "us": round(1000 * ms, 2),
                      "us_median": round(1000 * statistics.median(per_op_ms[name]), 2),
+                     "us_p10": round(1000 * qs[0], 2), "us_p90": round(1000 * qs[-1], 2),
                      "GBps": round(gbs, 1), "pct_of_8TBps": round(100 * gbs / NOMINAL_HBM_GBS, 2),
                      f"frac_of_{peak_kind}": round(gbs / peak, 4)}
     dominant = ops[dom_i]
@@ -689,8 +761,10 @@ def run_gpu(args, rank, world, local_rank):
     if not args.no_extras:
         extras["ops_alone"] = ops_alone(step)
         extras["latency_us"] = latency_sweep(rr, stream)
+        extras["small_config"] = small_config_latency(rr, stream)
         extras["fsdp_28_layers"] = fsdp_28_layers(rr, stream)
         extras["allgather_sweep"] = ag_sweep(rr, stream)
+        extras["allgather_dtypes"] = ag_sweep_dtypes(rr, stream)
         extras["overlap_gemm"] = overlap_gemm(rr, stream)
 
     line = {
