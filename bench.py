@@ -760,9 +760,9 @@ def run_gpu(args, rank, world, local_rank):
     extras = {}
     if not args.no_extras:
         extras["ops_alone"] = ops_alone(step)
+        extras["fsdp_28_layers"] = fsdp_28_layers(rr, stream)
         extras["latency_us"] = latency_sweep(rr, stream)
         extras["small_config"] = small_config_latency(rr, stream)
-        extras["fsdp_28_layers"] = fsdp_28_layers(rr, stream)
         extras["allgather_sweep"] = ag_sweep(rr, stream)
         extras["allgather_dtypes"] = ag_sweep_dtypes(rr, stream)
         extras["overlap_gemm"] = overlap_gemm(rr, stream)
