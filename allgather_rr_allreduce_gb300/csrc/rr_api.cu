@@ -31,7 +31,7 @@ struct rr_signal_pad {
     int64_t round_bytes;  // 0 = automatic
     int inject;        // -1 or rank*4 + barrier
     int blocks_override;
-    int engine;        // gathers: 0 auto, 1 ldst, 2 tma, 3 copy engines
+    int engine;        // gathers: 0 auto (= 1), 1 ldst, 2 tma, 3 copy engines
     int reduce_engine; // one-shot with copy_mode off: 0 auto, 1 ldst, 2 tma
     int twoshot_mode;  // 0 auto, 1 pull (middle barrier), 2 push (owner broadcasts)
     int iters;         // in-launch iterations per call (test mode; 1 = off)
@@ -449,7 +449,9 @@ rr_status run_gather(rr_signal_pad *pad, Args &a, int64_t shard, bool list, cuda
 {
     rr_status st = check_device(pad);
     if (st != RR_OK) return st;
-    const int engine = pad->engine == 0 ? 2 : pad->engine;
+    // automatic: loads/stores (with the per-rank tile interleaving they match
+    // or beat the bulk-copy engine at every size, 1 KiB .. 512 MiB per rank)
+    const int engine = pad->engine == 0 ? 1 : pad->engine;
     const bool iterate = iterating(pad);
     if (iterate) {
         st = check_iterating(pad);

@@ -498,8 +498,9 @@ def ag_sweep(rr, stream):
                  for x, y in bufs]
         count = 400 if nbytes <= (1 << 20) else (60 if nbytes <= (64 << 20) else 10)
         count = max(count, sets)
-        for c in calls:
-            c()
+        for _ in range(1 if nbytes <= (64 << 20) else 3):  # fresh buffers: warm them first
+            for c in calls:
+                c()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
@@ -539,8 +540,7 @@ def fsdp_28_layers(rr, stream):
         calls.append(rr.bound_call("rr_allgather_param_contiguous", [x[r].data_ptr() for r in range(W)],
                                    [y.data_ptr()] + [None] * (W - 1), W, sp, len(splits), rr.RR_BF16,
                                    pad, stream.cuda_stream))
-    times = []
-    for rep in range(4):
+    def one_pass():
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -548,15 +548,23 @@ def fsdp_28_layers(rr, stream):
             c()
         e1.record(stream)
         e1.synchronize()
-        if rep:
-            times.append(e0.elapsed_time(e1))
+        return e0.elapsed_time(e1)
+
+    # A training step gathers the same persistent buffers every step: the
+    # figure is the steady state after 8 untimed passes; the first pass over
+    # the freshly made layers is reported beside it.
+    first = one_pass()
+    for _ in range(8):
+        one_pass()
+    ms = min(one_pass() for _ in range(4))
     pad.status(stream)
     pad.close()
-    ms = min(times)
     total = cfg["layers"] * 2 * W * S * EB
     return {"ms": round(ms, 4), "GBps": round(total / ms / 1e6, 1), "bytes": total,
             "pct_of_8TBps": round(100 * total / ms / 1e6 / NOMINAL_HBM_GBS, 2),
-            "us_per_layer": round(1000 * ms / cfg["layers"], 2)}
+            "us_per_layer": round(1000 * ms / cfg["layers"], 2),
+            "first_pass_us_per_layer": round(1000 * first / cfg["layers"], 2),
+            "how": "steady state: best of 4 passes after 8 untimed passes over the 28 layers"}
 
 
 def overlap_gemm(rr, stream, n_ag=40, mkn=8192):
@@ -735,7 +743,11 @@ def run_gpu(args, rank, world, local_rank):
     e1 = run_e2e_pipelined([step, step_b], e2e_steps_p, e0)
     torch.cuda.synchronize()
     step_b.pad.status(stream)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps_p, world)
+    e2e_pipe_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps_p, world)
+    # Whether overlapping the two copy directions pays depends on the host
+    # (on some boxes concurrent copies in and out are slower than serial
+    # ones): both schedules are timed, the faster one is the figure.
+    e2e_ms = min(e2e_pipe_ms, e2e_serial_ms)
     bi, bo = step.e2e_bytes()
 
     if rank != 0:
@@ -795,13 +807,17 @@ def run_gpu(args, rank, world, local_rank):
                     "(each pair adds a few us to its op); value uses the timed steps",
         "e2e": {"value": round(world * step_bytes / e2e_ms / 1e6, 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-                "steps": e2e_steps_p,
+                "schedule": "pipelined" if e2e_pipe_ms <= e2e_serial_ms else "serial",
                 "how": "public API calls on device buffers; every step copies all inputs host->device "
-                       "from pinned memory and all outputs device->host; consecutive steps alternate "
-                       "between two buffer sets so that one step's copies in overlap the previous "
-                       "step's copies out (two copy streams)",
+                       "from pinned memory and all outputs device->host.  Two schedules are timed and "
+                       "the faster is the figure: serial (copies in, the step, copies out, on one "
+                       "stream) and pipelined (steps alternate between two buffer sets so that one "
+                       "step's copies in overlap the previous step's copies out, two copy streams)",
                 "serial_ms_per_step": round(e2e_serial_ms, 3),
-                "serial_value": round(world * step_bytes / e2e_serial_ms / 1e6, 1)},
+                "serial_value": round(world * step_bytes / e2e_serial_ms / 1e6, 1),
+                "pipelined_ms_per_step": round(e2e_pipe_ms, 3),
+                "pipelined_value": round(world * step_bytes / e2e_pipe_ms / 1e6, 1),
+                "steps": {"serial": e2e_steps, "pipelined": e2e_steps_p}},
         "gpu_launches": len(ops) * args.steps,
         "clocks": clocks,
         "cpu_baseline": None,
