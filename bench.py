@@ -824,7 +824,7 @@ def run_gpu(args, rank, world, local_rank):
     }
     line.update(extras)
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(sample_div=1, reps=3)
+        line["cpu_baseline"] = cpu_baseline()
     return line
 
 
@@ -846,17 +846,58 @@ def _cpu_workload(sample_div, seed):
     return n, splits, ins
 
 
-def _cpu_step(oracle, n, splits, ins):
+def _cpu_step(oracle, n, splits, ins, threads=1):
     # The oracle's definition of each op.  Staging (copy_mode) is a copy of
-    # each input into its registered buffer, then the same sum.
-    oracle.allreduce(ins["os_off"], "bf16")
+    # each input into its registered buffer, then the same sum.  threads > 1
+    # runs the oracle's multi-threaded entry points (the same loops with the
+    # element range split over host threads; same bits).
+    if threads == 1:
+        ar, ag, pc = oracle.allreduce, oracle.allgather_rank_major, oracle.allgather_param_contiguous
+        args = ()
+    else:
+        ar, ag, pc = oracle.allreduce_mt, oracle.allgather_rank_major_mt, oracle.allgather_param_contiguous_mt
+        args = (threads,)
+    ar(ins["os_off"], "bf16", *args)
     staged = [np.array(a, copy=True) for a in ins["os_on"]]
-    oracle.allreduce(staged, "bf16")
-    oracle.allreduce(ins["ts_off"], "bf16")
+    ar(staged, "bf16", *args)
+    ar(ins["ts_off"], "bf16", *args)
     staged = [np.array(a, copy=True) for a in ins["ts_on"]]
-    oracle.allreduce(staged, "bf16")
-    oracle.allgather_rank_major(ins["ag"], "bf16")
-    oracle.allgather_param_contiguous(ins["pc"], splits, "bf16")
+    ar(staged, "bf16", *args)
+    ag(ins["ag"], "bf16", *args)
+    pc(ins["pc"], splits, "bf16", *args)
+
+
+def host_cores():
+    """Cores this process may run on, and the CPU model name."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if model is None:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.startswith("Model name:"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    return cores, model
+
+
+def _time_cpu_steps(oracle, n, splits, ins, threads, warmup, steps):
+    for _ in range(warmup):
+        _cpu_step(oracle, n, splits, ins, threads)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        _cpu_step(oracle, n, splits, ins, threads)
+    return (time.perf_counter() - t0) / steps
 
 
 def _cpu_bytes(n, splits):
@@ -867,20 +908,25 @@ def _cpu_bytes(n, splits):
     return (W * nb + nb) + (2 * W * nb + nb) + 2 * W * nb + 3 * W * nb + 2 * W * nb + 2 * W * pc
 
 
-def cpu_baseline(sample_div=8, reps=1):
+def cpu_baseline(sample_div=4, reps=3):
+    """The oracle on the host: every core (the multi-threaded entry points,
+    one thread per core), and one core beside it, on a sample of the step."""
     import oracle
     oracle.lib()
+    cores, model = host_cores()
     n, splits, ins = _cpu_workload(sample_div, seed=7000)
-    _cpu_step(oracle, n, splits, ins)
-    t0 = time.perf_counter()
-    for _ in range(reps):
-        _cpu_step(oracle, n, splits, ins)
-    dt = (time.perf_counter() - t0) / reps
     b = _cpu_bytes(n, splits)
-    return {"value": round(b / dt / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"one full step at 1/{sample_div} of every op's elements per rank "
-                      f"({n} elements per rank, layer splits / {sample_div}), {reps} rep(s), "
-                      f"{dt:.2f} s per step, single-threaded C"}
+    dt_all = _time_cpu_steps(oracle, n, splits, ins, cores, 1, reps)
+    dt_one = _time_cpu_steps(oracle, n, splits, ins, 1, 1, reps)
+    return {"value": round(b / dt_all / 1e9, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "cpu_model": model,
+            "sample": f"one step at 1/{sample_div} of every op's elements per rank ({n} elements per rank, "
+                      f"layer splits / {sample_div}), {reps} timed rep(s) after one warm-up: {dt_all:.3f} s per "
+                      f"step on {cores} threads (the oracle's loops with the element range split over "
+                      f"threads, same bits), {dt_one:.3f} s on one",
+            "single_core": {"value": round(b / dt_one / 1e9, 3), "unit": "GB/s", "cores": 1,
+                            "s_per_step": round(dt_one, 4)},
+            "s_per_step": round(dt_all, 4)}
 
 
 def run_reference(args, rank, world):
@@ -888,27 +934,26 @@ def run_reference(args, rank, world):
         return None
     import oracle
     oracle.lib()
+    cores, model = host_cores()
     sample_div = 16
     n, splits, ins = _cpu_workload(sample_div, seed=8000)
-    for _ in range(args.warmup):
-        _cpu_step(oracle, n, splits, ins)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        _cpu_step(oracle, n, splits, ins)
-    dt = (time.perf_counter() - t0) / args.steps
+    dt = _time_cpu_steps(oracle, n, splits, ins, cores, args.warmup, args.steps)
+    dt_one = _time_cpu_steps(oracle, n, splits, ins, 1, 1, 3)
     b = _cpu_bytes(n, splits)
     v = b / dt / 1e9
     sample = (f"each step: the whole hot path at 1/{sample_div} of every op's elements per rank "
-              f"({n} bf16 per rank, layer splits / {sample_div}); single-threaded C oracle")
+              f"({n} bf16 per rank, layer splits / {sample_div}); C oracle on {cores} threads (its loops "
+              f"with the element range split over threads, same bits)")
     return {
         "impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * dt, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; N(0,1) ranks, N(0,0.02) layer shards)",
         "config": {"workload": f"W8_bf16_2^24 hot path, sampled at 1/{sample_div}", "W": W,
-                   "numel_per_rank": n, "parallelism": "CPU oracle, rank 0 only"},
-        "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                   "numel_per_rank": n, "parallelism": f"CPU oracle on {cores} host threads, rank 0 only"},
+        "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "cpu_model": model, "sample": sample,
+                         "single_core": {"value": round(b / dt_one / 1e9, 3), "unit": "GB/s", "cores": 1}},
         "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }

@@ -43,8 +43,15 @@ def lib():
                                                         ctypes.POINTER(ctypes.c_int64), ctypes.c_int,
                                                         ctypes.c_int, vp]
         l.oracle_cast.argtypes = [vp, ctypes.c_int, vp, ctypes.c_int, ctypes.c_int64]
+        i32 = ctypes.c_int
+        l.oracle_allreduce_mt.argtypes = l.oracle_allreduce.argtypes + [i32]
+        l.oracle_allgather_rank_major_mt.argtypes = l.oracle_allgather_rank_major.argtypes + [i32]
+        l.oracle_allgather_param_contiguous_mt.argtypes = l.oracle_allgather_param_contiguous.argtypes + [i32]
+        l.oracle_max_threads.argtypes = []
         for f in (l.oracle_allreduce, l.oracle_allgather_rank_major,
-                  l.oracle_allgather_param_contiguous, l.oracle_cast):
+                  l.oracle_allgather_param_contiguous, l.oracle_cast, l.oracle_allreduce_mt,
+                  l.oracle_allgather_rank_major_mt, l.oracle_allgather_param_contiguous_mt,
+                  l.oracle_max_threads):
             f.restype = ctypes.c_int
         _lib = l
     return _lib
@@ -112,6 +119,51 @@ def allgather_param_contiguous(inputs, splits, dtype):
                                                    ELEM_SIZE[dtype],
                                                    out.ctypes.data if out.size else None),
            "param-contiguous allgather")
+    return out
+
+
+def max_threads():
+    """Host threads the multi-threaded entry points use by default (1 when
+    the library was built without OpenMP)."""
+    return int(lib().oracle_max_threads())
+
+
+def allreduce_mt(inputs, dtype, threads=0):
+    """allreduce() with the element range split over host threads: the same
+    additions in the same order per element, so the same bits."""
+    ins = _as_storage(inputs, dtype)
+    n = ins[0].size
+    assert all(a.size == n for a in ins)
+    out = np.empty(n, dtype=NP_STORAGE[dtype])
+    _check(lib().oracle_allreduce_mt(_ptrs(ins), len(ins), n, DTYPES[dtype],
+                                     out.ctypes.data if n else None, int(threads)), "allreduce_mt")
+    return out
+
+
+def allgather_rank_major_mt(inputs, dtype, threads=0):
+    """allgather_rank_major() with the copies split over host threads."""
+    ins = _as_storage(inputs, dtype)
+    n = ins[0].size
+    assert all(a.size == n for a in ins)
+    out = np.empty(n * len(ins), dtype=NP_STORAGE[dtype])
+    _check(lib().oracle_allgather_rank_major_mt(_ptrs(ins), len(ins), n, ELEM_SIZE[dtype],
+                                                out.ctypes.data if out.size else None, int(threads)),
+           "allgather_mt")
+    return out
+
+
+def allgather_param_contiguous_mt(inputs, splits, dtype, threads=0):
+    """allgather_param_contiguous() with the copies split over host threads."""
+    ins = _as_storage(inputs, dtype)
+    splits = [int(s) for s in splits]
+    total = sum(splits)
+    assert all(a.size == total for a in ins)
+    sp = (ctypes.c_int64 * max(1, len(splits)))(*splits)
+    out = np.empty(total * len(ins), dtype=NP_STORAGE[dtype])
+    _check(lib().oracle_allgather_param_contiguous_mt(_ptrs(ins), len(ins), sp, len(splits),
+                                                      ELEM_SIZE[dtype],
+                                                      out.ctypes.data if out.size else None, int(threads)),
+           "param-contiguous allgather_mt")
     return out
 
 

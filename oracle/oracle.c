@@ -34,10 +34,19 @@
  * definitions and the bfloat16 definition (the upper 16 bits of a binary32).
  * Build with -ffp-contract=off and without -ffast-math so that every float
  * addition is one IEEE binary32 addition.
+ *
+ * The *_mt entry points run the same loops with the element (or byte) index
+ * range split over host threads (OpenMP, when the compiler offers it).  Each
+ * output element is still computed by one thread with the same additions in
+ * the same order, so their outputs are bit-identical to the single-threaded
+ * ones; they exist only so that the CPU baseline can use every host core.
  */
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 /* element type codes used by this oracle's entry points */
 enum { ORACLE_BF16 = 0, ORACLE_FP16 = 1, ORACLE_FP32 = 2, ORACLE_INT32 = 3 };
@@ -221,6 +230,136 @@ int oracle_allgather_param_contiguous(const void *const *in, int W, const int64_
         for (int r = 0; r < W; ++r)
             memcpy((char *)out + (size_t)(O * W + (int64_t)r * E) * (size_t)esize,
                    (const char *)in[r] + (size_t)O * (size_t)esize, (size_t)E * (size_t)esize);
+        O += E;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------ multi-threaded
+ * The loops above, with the index range split over `threads` host threads
+ * (<= 0: the OpenMP default).  Same per-element arithmetic, same order. */
+
+/* Threads an *_mt call with threads <= 0 uses (1 without OpenMP). */
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+int oracle_allreduce_mt(const void *const *in, int W, int64_t numel, int dtype, void *out, int threads)
+{
+    if (W < 1 || numel < 0 || !in || elem_size(dtype) == 0) return -1;
+    if (numel == 0) return 0;
+    if (!out) return -1;
+    for (int r = 0; r < W; ++r)
+        if (!in[r]) return -1;
+    if (threads <= 0) threads = oracle_max_threads();
+    (void)threads;
+    if (dtype == ORACLE_INT32) {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(threads)
+#endif
+        for (int64_t i = 0; i < numel; ++i) {
+            uint32_t acc = (uint32_t)((const int32_t *)in[0])[i];
+            for (int r = 1; r < W; ++r) acc += (uint32_t)((const int32_t *)in[r])[i];
+            ((uint32_t *)out)[i] = acc;
+        }
+        return 0;
+    }
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(threads)
+#endif
+    for (int64_t i = 0; i < numel; ++i) {
+        float acc = load_as_f32(in[0], dtype, i);
+        for (int r = 1; r < W; ++r) acc = acc + load_as_f32(in[r], dtype, i);
+        store_from_f32(out, dtype, i, acc);
+    }
+    return 0;
+}
+
+/* One byte-range copy of a gather, cut into 1 MiB pieces spread over threads. */
+struct copy_piece {
+    char *dst;
+    const char *src;
+    size_t len;
+};
+
+static void run_pieces(const struct copy_piece *c, int n, int threads)
+{
+    (void)threads;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(threads)
+#endif
+    for (int i = 0; i < n; ++i) memcpy(c[i].dst, c[i].src, c[i].len);
+}
+
+#define ORACLE_PIECE ((size_t)1 << 20)
+
+static int copy_ranges_mt(char *const *dst, const char *const *src, const size_t *len, int n, int threads)
+{
+    size_t pieces = 0;
+    for (int i = 0; i < n; ++i) pieces += (len[i] + ORACLE_PIECE - 1) / ORACLE_PIECE;
+    if (pieces == 0) return 0;
+    if (pieces > (size_t)1 << 30) return -1;
+    struct copy_piece buf[256];
+    size_t k = 0;
+    for (int i = 0; i < n; ++i)
+        for (size_t o = 0; o < len[i]; o += ORACLE_PIECE) {
+            buf[k].dst = dst[i] + o;
+            buf[k].src = src[i] + o;
+            buf[k].len = len[i] - o < ORACLE_PIECE ? len[i] - o : ORACLE_PIECE;
+            if (++k == 256) {
+                run_pieces(buf, 256, threads);
+                k = 0;
+            }
+        }
+    if (k) run_pieces(buf, (int)k, threads);
+    return 0;
+}
+
+int oracle_allgather_rank_major_mt(const void *const *in, int W, int64_t numel, int esize, void *out,
+                                   int threads)
+{
+    if (W < 1 || numel < 0 || !in || (esize != 2 && esize != 4)) return -1;
+    if (numel == 0) return 0;
+    if (!out) return -1;
+    if (threads <= 0) threads = oracle_max_threads();
+    for (int r = 0; r < W; ++r) {
+        if (!in[r]) return -1;
+        char *d = (char *)out + (size_t)r * (size_t)numel * (size_t)esize;
+        const char *s = (const char *)in[r];
+        size_t len = (size_t)numel * (size_t)esize;
+        if (copy_ranges_mt(&d, &s, &len, 1, threads)) return -1;
+    }
+    return 0;
+}
+
+int oracle_allgather_param_contiguous_mt(const void *const *in, int W, const int64_t *splits, int S,
+                                         int esize, void *out, int threads)
+{
+    if (W < 1 || S < 0 || !in || (esize != 2 && esize != 4) || (S && !splits)) return -1;
+    int64_t total = 0;
+    for (int s = 0; s < S; ++s) {
+        if (splits[s] < 0) return -1;
+        total += splits[s];
+    }
+    if (total == 0) return 0;
+    if (!out) return -1;
+    for (int r = 0; r < W; ++r)
+        if (!in[r]) return -1;
+    if (threads <= 0) threads = oracle_max_threads();
+    int64_t O = 0;
+    for (int s = 0; s < S; ++s) {
+        int64_t E = splits[s];
+        for (int r = 0; r < W; ++r) {
+            char *d = (char *)out + (size_t)(O * W + (int64_t)r * E) * (size_t)esize;
+            const char *src = (const char *)in[r] + (size_t)O * (size_t)esize;
+            size_t len = (size_t)E * (size_t)esize;
+            if (copy_ranges_mt(&d, &src, &len, 1, threads)) return -1;
+        }
         O += E;
     }
     return 0;

@@ -58,12 +58,24 @@ def _quick_pins():
     yield lambda: pins.test_rank_major_matches_torch_cat(om, "int32", 3, 1001)
 
 
-def _build_mutant(tmp_path, name, old, new):
+# oracle.c holds the single-threaded definitions first, then the multi-threaded
+# copies of the same loops after this marker.
+MT_MARK = "/* ------------------------------------------------------------ multi-threaded"
+
+
+def _build_mutant(tmp_path, name, old, new, part="single"):
     text = open(SRC).read()
-    assert text.count(old) == 1, f"mutant {name}: anchor not found exactly once"
-    src = tmp_path / f"{name}.c"
-    src.write_text(text.replace(old, new))
-    so = tmp_path / f"{name}.so"
+    head, mark, tail = text.partition(MT_MARK)
+    assert mark, "multi-threaded section marker missing"
+    if part == "single":
+        assert head.count(old) == 1, f"mutant {name}: anchor not found exactly once"
+        head = head.replace(old, new)
+    else:
+        assert tail.count(old) == 1, f"mutant {name}: anchor not found exactly once in the threaded loops"
+        tail = tail.replace(old, new)
+    src = tmp_path / f"{name}_{part}.c"
+    src.write_text(head + mark + tail)
+    so = tmp_path / f"{name}_{part}.so"
     subprocess.run(["gcc", "-std=c99", "-O2", "-fPIC", "-shared", "-ffp-contract=off",
                     "-o", str(so), str(src), "-lm"], check=True)
     return str(so)
@@ -96,3 +108,49 @@ def test_mutant_is_caught(tmp_path, name):
 def test_real_oracle_passes_quick_pins():
     for pin in _quick_pins():
         pin()
+
+
+# The same slips planted in the multi-threaded copies of the loops (where
+# their anchor occurs there): comparing the threaded entry points with the
+# single-threaded definitions, as tests/test_oracle_mt.py does, must catch them.
+MT_MUTANTS = sorted(n for n, (old, _) in MUTANTS.items()
+                    if open(SRC).read().partition(MT_MARK)[2].count(old) == 1)
+
+
+def test_threaded_mutants_exist():
+    assert len(MT_MUTANTS) >= 5, MT_MUTANTS
+
+
+@pytest.mark.parametrize("name", MT_MUTANTS)
+def test_threaded_mutant_is_caught(tmp_path, name):
+    import numpy as np
+    import workloads
+    old, new = MUTANTS[name]
+    mutant = ctypes.CDLL(_build_mutant(tmp_path, name, old, new, part="threaded"))
+    real = oracle.lib()
+    for fn in ("oracle_allreduce_mt", "oracle_allgather_rank_major_mt", "oracle_allgather_param_contiguous_mt"):
+        getattr(mutant, fn).argtypes = getattr(real, fn).argtypes
+        getattr(mutant, fn).restype = ctypes.c_int
+    caught = False
+    for dtype in ("bf16", "fp32", "int32"):
+        ins = workloads.rank_buffers(4, 1001, dtype, "int" if dtype == "int32" else "normal", seed_base=77)
+        st = [np.ascontiguousarray(a) for a in ins]
+        ptrs = (ctypes.c_void_p * 4)(*[a.ctypes.data for a in st])
+        out = np.empty(1001, dtype=st[0].dtype)
+        mutant.oracle_allreduce_mt(ptrs, 4, 1001, oracle.DTYPES[dtype], out.ctypes.data, 2)
+        caught |= not np.array_equal(out.view(np.uint8), oracle.allreduce(ins, dtype).view(np.uint8))
+        out = np.empty(4 * 1001, dtype=st[0].dtype)
+        mutant.oracle_allgather_rank_major_mt(ptrs, 4, 1001, oracle.ELEM_SIZE[dtype], out.ctypes.data, 2)
+        caught |= not np.array_equal(out.view(np.uint8), oracle.allgather_rank_major(ins, dtype).view(np.uint8))
+        splits = [300, 0, 701]
+        sp = (ctypes.c_int64 * 3)(*splits)
+        mutant.oracle_allgather_param_contiguous_mt(ptrs, 4, sp, 3, oracle.ELEM_SIZE[dtype], out.ctypes.data, 2)
+        caught |= not np.array_equal(out.view(np.uint8),
+                                     oracle.allgather_param_contiguous(ins, splits, dtype).view(np.uint8))
+    # W = 1 over every bf16 pattern: the sum is the input itself, -0 included
+    allbits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    one = (ctypes.c_void_p * 1)(allbits.ctypes.data)
+    out = np.empty(1 << 16, dtype=np.uint16)
+    mutant.oracle_allreduce_mt(one, 1, 1 << 16, oracle.DTYPES["bf16"], out.ctypes.data, 2)
+    caught |= not np.array_equal(out, oracle.allreduce([allbits], "bf16"))
+    assert caught, f"threaded mutant {name} gives the same bits as the definition"
