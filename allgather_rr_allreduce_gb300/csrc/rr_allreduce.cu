@@ -191,6 +191,9 @@ __device__ __forceinline__ void reduce_share(const ReduceArgs &a, int r, int64_t
 }
 
 // ------------------------------------------------------------------ one-shot
+// copy_mode off: tile size (vectors) of the block-interleaved work split; 0 =
+// contiguous chunk b split over the W blocks of index b (reduce_share).
+constexpr int64_t kOneshotTileVec = 1024;
 // Block b of every rank works on chunk b (vectors part_range(nvec, B, b); the
 // ragged tail belongs to the last chunk).
 //  copy_mode off: ARRIVE barrier (block 0 of every rank has started, so every
@@ -243,7 +246,20 @@ __device__ __forceinline__ void oneshot_kernel_body(const ReduceArgs &a, const S
     } else {
         if (b == 0) emit(sig, RR_BARRIER_ARRIVE, r, 0);
         if (!wait(sig, RR_BARRIER_ARRIVE, r, 0, &s_ok)) return;
-        reduce_share<Op, WMAX, false>(a, r, v0, v1);
+        if constexpr (kOneshotTileVec > 0) {
+            // Tiles of kOneshotTileVec vectors of every kept output, dealt to
+            // all W * B blocks in turn: the blocks move through one window of
+            // each rank buffer together.
+            const int64_t tpo = (a.nvec + kOneshotTileVec - 1) / kOneshotTileVec;
+            const int64_t ntiles = (int64_t)a.nout * tpo;
+            for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+                const int m = (int)(t / tpo);
+                const int64_t s0 = (t - (int64_t)m * tpo) * kOneshotTileVec;
+                reduce_vectors<Op, WMAX, false>(a, a.out[a.qlist[m]], s0, min(a.nvec, s0 + kOneshotTileVec));
+            }
+        } else {
+            reduce_share<Op, WMAX, false>(a, r, v0, v1);
+        }
         if (has_tail)
             for (int m = r; m < a.nout; m += a.W)
                 for (int e = threadIdx.x; e < ntail; e += kReduceThreads)
@@ -582,113 +598,206 @@ __global__ void __launch_bounds__(kRtThreads, 1) oneshot_tma_kernel(const __grid
 // copy_mode with the staging done by a producer warp through the bulk-copy
 // engine, for the one-shot and for the two-shot with a broadcast allgather.
 //
-// Producer (lane 0 of the last warp): copies, round by round, everything
-// block b of any rank will read from rank r into rank_bufs[r] (one-shot:
-// round k of chunk b; two-shot: round k of chunk b of every owner's segment)
-// as 16 KiB tiles through a ring of shared-memory stages: cp.async.bulk
-// global -> shared completing on a `full` mbarrier, then cp.async.bulk shared
-// -> global in a bulk group.  Loads run kSwAhead tiles ahead of the stores.
-// After each store it lets at most kSwReading bulk groups still read shared
-// memory (stage recycling) and at most kSwLanding still land in global
-// memory; once every tile of a round has landed the round is published:
-// async-proxy fence, one release fence, the newest complete round's flag
-// (STAGE) stored to every listener.  Only this lane waits for the stores to
-// land.  A short landing window publishes a round soon after its last store
-// (measured at W=8 x 32 MiB: 4 groups beat 16 by 9-13 %).
-// Consumers (the other 16 warps): per round, each warp waits on its own for
-// round flag k of block b of every rank (no poll while an earlier poll
-// already showed it), then reduces its part of round k from the staged
-// buffers, which the producers wrote moments ago (L2).
+// Work is cut into pieces of P = round_vec vectors (16 KiB by default): the
+// one-shot has one range (the message), the two-shot W ranges (the owners'
+// segments).  Pieces are dealt to a rank's blocks in turn: block b takes
+// pieces b, b + B, b + 2B, ... of every range, so the B blocks of a rank move
+// through its buffers together (one moving window per rank instead of one
+// per block).  Round k of block b is piece b + kB of every range; a unit is
+// one (round, range) pair, numbered k * ranges + j.
+//
+// Producer (lane 0 of the warp after the consumers): stages, unit by unit, piece b + kB of range j
+// from inputs[r] into rank_bufs[r], as tiles of up to 16 KiB through a ring
+// of shared-memory stages: cp.async.bulk global -> shared completing on a
+// `full` mbarrier, then cp.async.bulk shared -> global in a bulk group.  Loads
+// run kSwAhead tiles ahead of the stores.  After each store it lets at most
+// kSwReading bulk groups still read shared memory (stage recycling) and at
+// most kSwLanding still land in global memory; the count of units whose tiles
+// have all landed then goes, after an async-proxy fence, to the publisher
+// through shared memory.  Only this lane waits for the stores to land.
+// Publisher (lane 0 of the next warp): stores each new count to every listener
+// behind one release fence (STAGE round flags, read as "at least").  The
+// fence waits for the memory operations in flight from its warp, so it runs
+// in a warp of its own: in the producer's warp it would drain the bulk loads
+// in flight at every publication.
+// Poller (the last warp): polls the STAGE flags of block b of every rank (lane
+// p, rank p; relaxed loads, one acquire fence per step of progress: an
+// acquire load per poll costs the whole block memory bandwidth) and hands the
+// count of units that every rank has published to the consumers through
+// shared memory.
+// Consumers (the first warps, C of them): the block's share of the reduction is a list of
+// items in unit order (one-shot: the (output, vector) pairs of each piece
+// that fall to this rank's block b, see reduce_share; two-shot: the vectors of
+// the piece of the rank's own segment, each reduced once and stored into
+// every output).  Warp w takes items [32g, 32g + 32) for g = w, w + C, ...
+// (several such groups per pass, to keep 8 or 16 loads in flight per thread);
+// before a pass it reads the poller's count until it covers the pass's last
+// unit.  A unit is consumed a few microseconds after it is staged, while
+// its bytes are still in L2, and the last one leaves only one piece to
+// reduce after the staging ends.  The consumers never poll global flags
+// themselves: a GPU-scope acquire would first wait for their own output
+// stores still in flight.
 // The ragged tail is staged by the consumers before the roles split, so the
 // producer's first release covers it.  END barrier over the whole block.
-constexpr int kSwConsumerWarps = 16;
-constexpr int kSwConsumers = 32 * kSwConsumerWarps;
-constexpr int kSwThreads = kSwConsumers + 32;
+// Warp roles per kernel: consumer warps, then the producer, the publisher and
+// the poller.  The one-shot runs 12 consumer warps with 16 loads in flight per
+// thread (more registers per thread with fewer warps: 106 against 110 us at
+// W=8 x 32 MiB); the two-shot, whose consumers also store every sum W times,
+// runs 16 with 8 (149 us either way).
+template <bool kTwoShot>
+struct SwShape {
+    static constexpr int kConsumerWarps = kTwoShot ? 16 : 12;
+    static constexpr int kLoads = kTwoShot ? 8 : 16;  // loads in flight per consumer thread
+    static constexpr int kConsumers = 32 * kConsumerWarps;
+    static constexpr int kProducerWarp = kConsumerWarps;
+    static constexpr int kPublisherWarp = kConsumerWarps + 1;
+    static constexpr int kPollerWarp = kConsumerWarps + 2;
+    static constexpr int kThreads = kConsumers + 96;
+};
 constexpr int kSwStages = 12;
 constexpr int kSwAhead = 4;          // loads in flight ahead of the store being issued
 constexpr int kSwReading = 6;        // store groups allowed to be still reading shared memory
-constexpr int kSwLanding = 4;        // store groups allowed to be still landing in global memory
-constexpr int kSwRoundRing = 32;     // rounds of the last kSwRoundRing tiles are remembered
+constexpr int kSwLanding = 2;        // store groups allowed to be still landing in global memory
+constexpr int kSwUnitRing = 32;      // units of the last kSwUnitRing tiles are remembered
 constexpr int kSwTileBytes = 16384;
 constexpr int kSwSmem = kSwStages * kSwTileBytes;  // 192 KiB
 // The stage a new load reuses (tile t + kSwAhead - kSwStages) must have been
-// read by its store (tiles <= t - kSwReading), and the round of the oldest
+// read by its store (tiles <= t - kSwReading), and the unit of the oldest
 // tile not yet known to have landed must still be remembered.
 static_assert(kSwAhead + kSwReading <= kSwStages, "stage reused before its store read it");
-static_assert(kSwLanding + kSwAhead < kSwRoundRing, "round ring too short");
+static_assert(kSwLanding + kSwAhead < kSwUnitRing, "unit ring too short");
 
 template <class Op, int WMAX, bool kTwoShot>
 __device__ __forceinline__ void staged_kernel_body(const ReduceArgs &a, const SignalArgs &sig)
 {
     extern __shared__ __align__(128) unsigned char stages[];
     __shared__ __align__(8) uint64_t full[kSwStages];
-    __shared__ int tile_round[kSwRoundRing];
+    __shared__ int tile_unit[kSwUnitRing];
     __shared__ int64_t tile_off[kSwStages];   // byte offset within the rank buffer
     __shared__ uint32_t tile_len[kSwStages];
-    __shared__ int64_t s_c0[RR_MAX_WORLD], s_c1[RR_MAX_WORLD];
-    __shared__ int s_ok, s_fail, s_R;
+    __shared__ int64_t s_r0[RR_MAX_WORLD], s_r1[RR_MAX_WORLD];  // ranges, in vectors
+    __shared__ int s_ok, s_fail;
+    __shared__ int s_landed;  // units whose tiles have all landed (producer -> publisher)
+    __shared__ int s_avail;   // units every rank's block b has published (poller -> consumers)
     const int W = a.W;
-    const int r = blockIdx.x / a.B;
-    const int b = blockIdx.x - r * a.B;
+    const int B = a.B;
+    const int r = blockIdx.x / B;
+    const int b = blockIdx.x - r * B;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool last = b == a.B - 1;
     const int64_t t0 = a.nvec * Op::kEPV;
     const int ntail = (int)(a.numel - t0);
-    const bool has_tail = last && ntail > 0;
+    const bool has_tail = b == B - 1 && ntail > 0;
     const int64_t P = a.round_vec;
     const int nranges = kTwoShot ? W : 1;
 
-    // Chunk b: one-shot, the block's share of the message; two-shot, chunk
-    // b of every owner's segment (s_c0/s_c1 indexed by owner).
     if ((int)threadIdx.x < nranges) {
-        int64_t c0, c1;
-        if (kTwoShot) owned_chunk(a.nvec, W, a.B, threadIdx.x, b, c0, c1);
-        else part_range(a.nvec, a.B, b, c0, c1);
-        s_c0[threadIdx.x] = c0;
-        s_c1[threadIdx.x] = c1;
+        int64_t s0 = 0, s1 = a.nvec;
+        if (kTwoShot) owned_segment(a.nvec, W, threadIdx.x, s0, s1);
+        s_r0[threadIdx.x] = s0;
+        s_r1[threadIdx.x] = s1;
     }
     if (threadIdx.x == 0) {
         for (int i = 0; i < kSwStages; ++i) mbar_init(&full[i], 1);
         fence_mbar_init();
         s_fail = 0;
+        s_landed = 0;
+        s_avail = 0;
     }
     if (has_tail) copy_tail<Op::kBytes>(a.in[r], a.buf[r], t0, ntail);
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int64_t longest = 0;
-        for (int j = 0; j < nranges; ++j) longest = max(longest, s_c1[j] - s_c0[j]);
-        int R = (int)((longest + P - 1) / P);
-        if (R == 0 && has_tail) R = 1;
-        s_R = R;
-    }
-    __syncthreads();
-    const int R = s_R;
+    // Range 0 is the longest (segments are full up to the short or empty last
+    // ones).  A block with a tail but no piece still publishes one unit.
+    int units = staged_rounds(s_r1[0] - s_r0[0], P, B, b) * nranges;
+    if (units == 0 && has_tail) units = 1;
 
-    if (warp == kSwConsumerWarps) {
-        if (lane == 0) {
-            // tile walk: round k, range j, byte position inside the range
-            int k = 0, j = 0;
-            int64_t pos = 0;
-            auto next_tile = [&](int &kr, int64_t &off, uint32_t &len) -> bool {
-                while (k < R) {
-                    if (j < nranges) {
-                        const int64_t c1 = s_c1[j];
-                        const int64_t rs = min(c1, s_c0[j] + (int64_t)k * P) * 16;
-                        const int64_t re = min(c1, s_c0[j] + (int64_t)(k + 1) * P) * 16;
-                        if (rs + pos < re) {
-                            off = rs + pos;
-                            const int64_t left = re - off;
-                            len = (uint32_t)(left < kSwTileBytes ? left : kSwTileBytes);
-                            pos += len;
-                            kr = k;
-                            return true;
-                        }
-                        ++j;
-                        pos = 0;
-                        continue;
+    using Shape = SwShape<kTwoShot>;
+    constexpr int kSwConsumerWarps = Shape::kConsumerWarps;
+    constexpr int kSwConsumers = Shape::kConsumers;
+    if (warp == Shape::kPollerWarp) {
+        // Bounded: gives up after the pad's timeout without progress, at once
+        // when the pad's abort word or the block's failure flag is set.
+        const uint64_t *slots = round_slot(sig, r, 0, b, 0);
+        int have = 0;
+        uint64_t t_last = global_ns();
+        for (uint32_t spins = 0; have < units; ++spins) {
+            int h = 0x7fffffff;
+            if (lane < W) {
+                const int64_t d = (int64_t)(ld_flag64_relaxed(slots + lane) - sig.rbase);
+                h = d < 0 ? 0 : (d > 0x7fffffff ? 0x7fffffff : (int)d);
+            }
+            const int mn = __reduce_min_sync(0xffffffffu, h);
+            if (mn > have) {
+                // relaxed loads that saw the release, then an acquire fence:
+                // lanes 0..W-1 acquire; the warp barrier orders their view
+                // before lane 0's release to the consumers.  (An acquire load
+                // per poll would cost the whole block memory bandwidth.)
+                fence_acquire_gpu();
+                __syncwarp();
+                have = mn;
+                if (lane == 0) st_shared_release(&s_avail, have);
+                t_last = global_ns();
+                spins = 0;
+                continue;
+            }
+            if ((spins & 31u) == 31u) {
+                const bool stop = lane == 0 && (ld_relaxed(sig.status + kStAbort) != 0u ||
+                                                *(volatile int *)&s_fail != 0);
+                const bool late = (global_ns() - t_last) > sig.timeout_ns;
+                if (__any_sync(0xffffffffu, stop || late)) {
+                    if (lane == 0) {
+                        if (late) record_timeout(sig, RR_BARRIER_STAGE, r, b);
+                        *(volatile int *)&s_fail = 1;
                     }
-                    ++k;
-                    j = 0;
+                    break;
+                }
+            }
+            if (spins >= 4) __nanosleep(32);
+        }
+    } else if (warp == Shape::kPublisherWarp) {
+        if (lane == 0) {
+            // Publish every new count of landed units; stop once all are out or
+            // the producer failed.  Bounded: gives up after the pad's timeout
+            // without progress.
+            int pub = 0;
+            uint64_t t_last = global_ns();
+            for (uint32_t spins = 0; pub < units; ++spins) {
+                const int v = ld_shared_acquire(&s_landed);
+                if (v > pub) {
+                    emit_round_single(sig, 0, r, b, v - 1);
+                    pub = v;
+                    t_last = global_ns();
+                    spins = 0;
+                    continue;
+                }
+                if (*(volatile int *)&s_fail) break;
+                if ((spins & 63u) == 63u && (global_ns() - t_last) > sig.timeout_ns) {
+                    record_timeout(sig, RR_BARRIER_STAGE, r, b);
+                    *(volatile int *)&s_fail = 1;
+                    break;
+                }
+                if (spins >= 8) __nanosleep(64);
+            }
+        }
+    } else if (warp == Shape::kProducerWarp) {
+        if (lane == 0) {
+            // tile walk: unit u, byte position inside the unit's piece
+            int u = 0;
+            int64_t pos = 0;
+            auto next_tile = [&](int &tu, int64_t &off, uint32_t &len) -> bool {
+                while (u < units) {
+                    const int k = kTwoShot ? u / nranges : u;
+                    const int j = kTwoShot ? u - k * nranges : 0;
+                    int64_t ps, pe;
+                    staged_piece(s_r0[j], s_r1[j], P, B, b, k, ps, pe);
+                    if (ps * 16 + pos < pe * 16) {
+                        off = ps * 16 + pos;
+                        const int64_t left = pe * 16 - off;
+                        len = (uint32_t)(left < kSwTileBytes ? left : kSwTileBytes);
+                        pos += len;
+                        tu = u;
+                        return true;
+                    }
+                    ++u;
                     pos = 0;
                 }
                 return false;
@@ -696,17 +805,17 @@ __device__ __forceinline__ void staged_kernel_body(const ReduceArgs &a, const Si
             const char *src = static_cast<const char *>(a.in[r]);
             char *dst = static_cast<char *>(a.buf[r]);
             // Inputs are read once (evict first); staged bytes are read back
-            // by the consumers of every rank within about a round (evict last).
+            // by the consumers of every rank within microseconds (evict last).
             const uint64_t read_once = l2_policy_evict_first();
             const uint64_t keep = l2_policy_evict_last();
             int issued = 0;
             auto issue = [&](int t) -> bool {
-                int kr;
+                int tu;
                 int64_t off;
                 uint32_t len;
-                if (!next_tile(kr, off, len)) return false;
+                if (!next_tile(tu, off, len)) return false;
                 const int st = t % kSwStages;
-                tile_round[t % kSwRoundRing] = kr;
+                tile_unit[t % kSwUnitRing] = tu;
                 tile_off[st] = off;
                 tile_len[st] = len;
                 mbar_expect_tx(&full[st], len);
@@ -714,14 +823,14 @@ __device__ __forceinline__ void staged_kernel_body(const ReduceArgs &a, const Si
                 return true;
             };
             while (issued < kSwAhead && issue(issued)) ++issued;
-            int published = 0;  // rounds whose flags are out
+            int published = 0;  // units handed to the publisher
             bool ok = true;
             for (int t = 0; t < issued; ++t) {
                 const int st = t % kSwStages;
                 if (!mbar_wait_bounded(sig, &full[st], (uint32_t)(t / kSwStages) & 1u)) {
                     ok = false;
-                    for (int u = t; u < issued; ++u)
-                        (void)mbar_wait_bounded(sig, &full[u % kSwStages], (uint32_t)(u / kSwStages) & 1u);
+                    for (int v = t; v < issued; ++v)
+                        (void)mbar_wait_bounded(sig, &full[v % kSwStages], (uint32_t)(v / kSwStages) & 1u);
                     break;
                 }
                 fence_async_shared();
@@ -733,11 +842,11 @@ __device__ __forceinline__ void staged_kernel_body(const ReduceArgs &a, const Si
                 bulk_wait_pending<kSwLanding>();
                 const int done = t - kSwLanding;
                 if (done >= 0) {
-                    // rounds before the round of tile done+1 are complete
-                    const int upto = (done + 1 < issued) ? tile_round[(done + 1) % kSwRoundRing] : -1;
+                    // units before the unit of tile done+1 are complete
+                    const int upto = (done + 1 < issued) ? tile_unit[(done + 1) % kSwUnitRing] : -1;
                     if (upto > published) {
                         fence_async_global();
-                        emit_round_single(sig, 0, r, b, upto - 1);
+                        st_shared_release(&s_landed, upto);
                         published = upto;
                     }
                 }
@@ -746,41 +855,98 @@ __device__ __forceinline__ void staged_kernel_body(const ReduceArgs &a, const Si
             bulk_wait_all();
             if (ok) {
                 fence_async_global();
-                if (published < R) emit_round_single(sig, 0, r, b, R - 1);
+                st_shared_release(&s_landed, units);
             } else {
-                s_fail = 1;
                 record_timeout(sig, RR_BARRIER_STAGE, r, b);
+                *(volatile int *)&s_fail = 1;
             }
         }
     } else {
-        // Each consumer warp waits for the round flags on its own (no block
-        // barrier per round) and skips the poll while earlier polls already
-        // showed the round published by every rank.
+        StagedItems items;
+        items.init(kTwoShot, s_r0[kTwoShot ? r : 0], s_r1[kTwoShot ? r : 0], P, B, b, r, W, a.nout);
+        const int64_t total = items.total;
+        constexpr int UG = WMAX >= Shape::kLoads ? 1 : Shape::kLoads / WMAX;  // groups per pass
+        // Wait until the poller's count passes unit `need` (bounded; false once
+        // the block failed or the pad's timeout passed).
         int avail = 0;
-        for (int k = 0; k < R; ++k) {
-            if (!warp_wait_round(sig, 0, r, b, k, avail)) {
-                if (lane == 0) s_fail = 1;
+        auto wait_unit = [&](int need) -> bool {
+            if (need < avail) return true;
+            const uint64_t tw = global_ns();
+            for (uint32_t spins = 0;; ++spins) {
+                // every lane acquires; the smallest count is one each lane saw
+                const int v = __reduce_min_sync(0xffffffffu, ld_shared_acquire(&s_avail));
+                if (v > need) {
+                    avail = v;
+                    return true;
+                }
+                if (__shfl_sync(0xffffffffu, *(volatile int *)&s_fail, 0)) return false;
+                if ((spins & 255u) == 255u &&
+                    __shfl_sync(0xffffffffu, (int)((global_ns() - tw) > sig.timeout_ns), 0))
+                    return false;
+                __nanosleep(20);
+            }
+        };
+        bool ok = true;
+        for (int64_t g0 = warp; ok && g0 * 32 < total; g0 += (int64_t)kSwConsumerWarps * UG) {
+            uint4 *dst[UG];
+            int64_t vv[UG];
+            int need = -1;
+#pragma unroll
+            for (int u = 0; u < UG; ++u) {
+                const int64_t i = (g0 + (int64_t)u * kSwConsumerWarps) * 32 + lane;
+                dst[u] = nullptr;
+                vv[u] = 0;
+                if (i < total) {
+                    int unit, m;
+                    items.item(i, unit, m, vv[u]);
+                    if (!kTwoShot) dst[u] = static_cast<uint4 *>(a.out[a.qlist[m]]);
+                    need = max(need, unit);
+                }
+            }
+            need = __reduce_max_sync(0xffffffffu, need);
+            if (!wait_unit(need)) {
+                ok = false;
                 break;
             }
-            if constexpr (kTwoShot) {
-                const int64_t c1 = s_c1[r];
-                const int64_t rs = min(c1, s_c0[r] + (int64_t)k * P);
-                const int64_t re = min(c1, rs + P);
-                reduce_vectors_bcast<Op, WMAX, true, kSwConsumers, true>(a, rs, re);
-                if (k == R - 1 && has_tail && r == W - 1)
-                    for (int e = threadIdx.x; e < ntail; e += kSwConsumers)
-                        combine_scalar_to<Op>(a.buf, W, a.out, W, t0 + e);
-            } else {
-                const int64_t c1 = s_c1[0];
-                const int64_t rs = min(c1, s_c0[0] + (int64_t)k * P);
-                const int64_t re = min(c1, rs + P);
-                reduce_share<Op, WMAX, true, kSwConsumers, true>(a, r, rs, re);
-                if (k == R - 1 && has_tail)
-                    for (int m = r; m < a.nout; m += W)
-                        for (int e = threadIdx.x; e < ntail; e += kSwConsumers)
-                            combine_scalar<Op>(a.buf, W, a.out[a.qlist[m]], t0 + e);
+            uint4 x[UG][WMAX];
+#pragma unroll
+            for (int u = 0; u < UG; ++u) {
+                const int64_t i = (g0 + (int64_t)u * kSwConsumerWarps) * 32 + lane;
+                if (i < total) {
+#pragma unroll
+                    for (int c = 0; c < WMAX; ++c)
+                        if (c < W) x[u][c] = ld_vec_stream(static_cast<const uint4 *>(a.buf[c]) + vv[u]);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < UG; ++u) {
+                const int64_t i = (g0 + (int64_t)u * kSwConsumerWarps) * 32 + lane;
+                if (i < total) {
+                    const uint4 y = combine<Op, WMAX>(x[u], W);
+                    if constexpr (kTwoShot) {
+#pragma unroll
+                        for (int q = 0; q < WMAX; ++q)
+                            if (q < W) st_vec_stream(static_cast<uint4 *>(a.out[q]) + vv[u], y);
+                    } else {
+                        st_vec_stream(dst[u] + vv[u], y);
+                    }
+                }
             }
         }
+        // The ragged tail, staged by every rank's block B-1 before its first
+        // publication.
+        if (ok && has_tail && (kTwoShot ? r == W - 1 : r < a.nout)) {
+            if (!wait_unit(0)) {
+                ok = false;
+            } else if constexpr (kTwoShot) {
+                for (int e = threadIdx.x; e < ntail; e += kSwConsumers) combine_scalar_to<Op>(a.buf, W, a.out, W, t0 + e);
+            } else {
+                for (int m = r; m < a.nout; m += W)
+                    for (int e = threadIdx.x; e < ntail; e += kSwConsumers)
+                        combine_scalar<Op>(a.buf, W, a.out[a.qlist[m]], t0 + e);
+            }
+        }
+        if (!ok && lane == 0) s_fail = 1;
     }
     __syncthreads();
     if (s_fail) return;
@@ -789,7 +955,7 @@ __device__ __forceinline__ void staged_kernel_body(const ReduceArgs &a, const Si
 }
 
 template <class Op, int WMAX, bool kTwoShot>
-__global__ void __launch_bounds__(kSwThreads, 1) staged_kernel(const __grid_constant__ ReduceArgs a)
+__global__ void __launch_bounds__(SwShape<kTwoShot>::kThreads, 1) staged_kernel(const __grid_constant__ ReduceArgs a)
 {
     const SignalArgs sig = begin_call(a.sig);
     staged_kernel_body<Op, WMAX, kTwoShot>(a, sig);
@@ -815,7 +981,7 @@ __global__ void __launch_bounds__(kReduceThreads, 2) twoshot_iter_kernel(const _
     });
 }
 template <int WMAX, bool kTwoShot>
-__global__ void __launch_bounds__(kSwThreads, 1) staged_iter_kernel(const __grid_constant__ ReduceArgs a)
+__global__ void __launch_bounds__(SwShape<kTwoShot>::kThreads, 1) staged_iter_kernel(const __grid_constant__ ReduceArgs a)
 {
     run_iterations(a, begin_call(a.sig), [](const ReduceArgs &ai, const SignalArgs &si) {
         staged_kernel_body<OpBF16, WMAX, kTwoShot>(ai, si);
@@ -834,7 +1000,7 @@ KernelChoice iter_reduce_kernel_for(bool twoshot, int W, bool copy_mode)
                                     : w == 4 ? (const void *)staged_iter_kernel<4, false>
                                     : w == 8 ? (const void *)staged_iter_kernel<8, false>
                                              : (const void *)staged_iter_kernel<16, false>);
-        return KernelChoice{fn, kSwThreads, kSwSmem};
+        return KernelChoice{fn, twoshot ? SwShape<true>::kThreads : SwShape<false>::kThreads, kSwSmem};
     }
     if (twoshot) {
         const void *fn = w == 2 ? (const void *)twoshot_iter_kernel<2>
@@ -911,7 +1077,7 @@ KernelChoice staged_kernel_for(rr_dtype dtype, int W, bool twoshot)
     case RR_FP32: fn = twoshot ? pick_staged_w<OpFP32, true>(W) : pick_staged_w<OpFP32, false>(W); break;
     default: fn = twoshot ? pick_staged_w<OpI32, true>(W) : pick_staged_w<OpI32, false>(W); break;
     }
-    return KernelChoice{fn, kSwThreads, kSwSmem};
+    return KernelChoice{fn, twoshot ? SwShape<true>::kThreads : SwShape<false>::kThreads, kSwSmem};
 }
 KernelChoice twoshot_kernel_for(rr_dtype dtype, int W, bool copy_mode, bool push)
 {

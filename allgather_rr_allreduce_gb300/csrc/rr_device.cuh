@@ -155,6 +155,14 @@ __device__ __forceinline__ uint64_t ld_flag64_acquire(const uint64_t *p)
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
+__device__ __forceinline__ uint64_t ld_flag64_relaxed(const uint64_t *p)
+{
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+// With a preceding relaxed load that read a release store: acquire.
+__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ uint64_t *round_slot(const SignalArgs &s, int listener, int kind, int b, int emitter)
 {
     return s.rflags + ((((size_t)listener * kRoundKinds + kind) * (size_t)s.Bmax + b) * (size_t)s.W + emitter);
@@ -194,52 +202,25 @@ __device__ __forceinline__ void emit_round_single(const SignalArgs &s, int kind,
     for (int p = 0; p < s.W; ++p) st_flag64_relaxed(round_slot(s, p, kind, b, r), s.rbase + (uint64_t)k + 1u);
 }
 
-// One warp waits, on its own, for round flag k of block b of every rank
-// (lane p < W polls emitter p with acquire loads; __syncwarp then orders the
-// other lanes' later reads after them).  `avail` is the warp's count of
-// rounds every emitter is known to have published: no poll while k < avail.
-// Bounded like wait_on; on failure lane 0 records the timeout and every lane
-// returns false.
-__device__ __forceinline__ bool warp_wait_round(const SignalArgs &s, int kind, int r, int b, int k, int &avail)
-{
-    if (k < avail) return true;
-    const int lane = threadIdx.x & 31;
-    const uint64_t *slots = round_slot(s, r, kind, b, 0);
-    const uint64_t t0 = global_ns();
-    uint32_t ns = 0;
-    for (uint32_t spins = 0;; ++spins) {
-        int have = 0x7fffffff;
-        if (lane < s.W) {
-            const int64_t d = (int64_t)(ld_flag64_acquire(slots + lane) - s.rbase);
-            have = d < 0 ? 0 : (d > 0x7fffffff ? 0x7fffffff : (int)d);
-        }
-        const int mn = __reduce_min_sync(0xffffffffu, have);
-        if (mn > k) {
-            __syncwarp();
-            avail = mn;
-            return true;
-        }
-        if ((spins & 31u) == 0u) {
-            const bool bad = (lane == 0 && ld_relaxed(s.status + kStAbort) != 0u) || spins > s.max_spins ||
-                             (global_ns() - t0) > s.timeout_ns;
-            if (__any_sync(0xffffffffu, bad)) {
-                if (lane == 0) record_timeout(s, round_barrier(kind), r, b);
-                return false;
-            }
-        }
-        if (spins >= 8) {
-            __nanosleep(ns);
-            ns = ns < 224 ? ns + 32 : 256;
-        }
-    }
-}
-
 // ------------------------------------------------------------ bulk copies
 // cp.async.bulk (TMA without a tensor map) between global and shared memory,
 // completion of loads counted on an mbarrier, stores tracked in bulk groups.
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// A count handed from one thread of a block to another through shared memory
+// (release / acquire at block scope): what the writer observed before the
+// store is visible to the reader after it reads the value.
+__device__ __forceinline__ void st_shared_release(int *p, int v)
+{
+    asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_shared_acquire(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.s32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
 }
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {
@@ -363,20 +344,20 @@ __device__ __forceinline__ SignalArgs begin_call(const SignalArgs &in)
 }
 
 // Every block passes here once, whatever path it took.  With the device
-// counter, the last block to arrive (all others have finished, so all have
-// read the counter) resets the tally and stores this call's generation for
-// the next call.
+// counter, the last block to arrive (all others have counted themselves, so
+// all have read the counter: every thread read it at the start and used the
+// value in the barriers since) resets the tally and stores this call's
+// generation for the next call.  No fence: the tally only has to follow the
+// reads, and the kernel boundary orders both stores before the next call.
 __device__ __forceinline__ void end_call(const SignalArgs &s)
 {
     if (!s.dev_gen) return;
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
         const uint32_t total = gridDim.x * gridDim.y * gridDim.z;
         if (atomicAdd(s.done, 1u) == total - 1u) {
             *(volatile uint32_t *)s.done = 0u;
             *(volatile uint64_t *)s.dev_gen = s.rbase >> kRoundBits;
-            __threadfence();
         }
     }
 }

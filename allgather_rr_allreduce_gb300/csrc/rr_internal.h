@@ -175,6 +175,104 @@ RR_HD void byte_region(int64_t bytes, int B, int b, int64_t &x0, int64_t &x1)
     x1 = e < bytes ? e : bytes;
 }
 
+// ------------------------------------------------- staged copy_mode pieces
+// The staged copy_mode kernel cuts each range (one-shot: the message; two-shot:
+// every owner's segment) into pieces of P vectors and deals them to a rank's B
+// blocks in turn: round k of block b is piece b + kB of every range, and unit
+// k * nranges + j is round k of range j.
+
+// Rounds of block b for a range of `len` vectors.
+RR_HD int staged_rounds(int64_t len, int64_t P, int B, int b)
+{
+    const int64_t T = (len + P - 1) / P;
+    return T > b ? (int)((T - b + B - 1) / B) : 0;
+}
+
+// Piece size P (vectors): 16 KiB by default (or option_bytes), in whole
+// granules, doubled until no block has 2^kRoundBits units or more (pieces of
+// `nranges` ranges of up to `seglen` vectors over B blocks).
+RR_HD int64_t staged_piece_vectors(int64_t option_bytes, int64_t seglen, int nranges, int B)
+{
+    int64_t p = option_bytes > 0 ? option_bytes / 16 : 1024;
+    p = ((p + kGranuleVec - 1) / kGranuleVec) * kGranuleVec;
+    if (p < kGranuleVec) p = kGranuleVec;
+    for (;;) {
+        if ((int64_t)staged_rounds(seglen, p, B, 0) * nranges < ((int64_t)1 << kRoundBits)) return p;
+        p *= 2;
+    }
+}
+
+// Vectors [ps, pe) of round k of block b in range [s0, s1) (pe <= ps: none).
+RR_HD void staged_piece(int64_t s0, int64_t s1, int64_t P, int B, int b, int k, int64_t &ps, int64_t &pe)
+{
+    ps = s0 + ((int64_t)b + (int64_t)k * B) * P;
+    pe = ps + P < s1 ? ps + P : s1;
+}
+
+// The reduction items of block (r, b), in unit order.  One-shot: round k's
+// piece of the message holds nout * L (output, vector) pairs, split evenly
+// over the W blocks of index b (reduce_share's split); this block takes its
+// share.  Two-shot: the vectors of round k's piece of rank r's own segment,
+// each reduced once and stored into every output.  Every round but the last
+// has c_full items, the last c_last.
+struct StagedItems {
+    int64_t own0, own1, P, c_full, c_last, L_last, n_first, total;
+    int K, B, b, r, W, nout, nranges;
+    bool twoshot;
+    RR_HD void init(bool twoshot_, int64_t own0_, int64_t own1_, int64_t P_, int B_, int b_, int r_, int W_,
+                    int nout_)
+    {
+        twoshot = twoshot_;
+        own0 = own0_;
+        own1 = own1_;
+        P = P_;
+        B = B_;
+        b = b_;
+        r = r_;
+        W = W_;
+        nout = nout_;
+        nranges = twoshot ? W : 1;
+        K = staged_rounds(own1 - own0, P, B, b);
+        c_full = c_last = L_last = 0;
+        if (K > 0) {
+            int64_t ps, pe;
+            staged_piece(own0, own1, P, B, b, K - 1, ps, pe);
+            L_last = pe - ps;
+            c_full = twoshot ? P : split_point((int64_t)nout * P, W, r + 1) - split_point((int64_t)nout * P, W, r);
+            c_last = twoshot ? L_last
+                             : split_point((int64_t)nout * L_last, W, r + 1) - split_point((int64_t)nout * L_last, W, r);
+        }
+        n_first = (int64_t)(K > 0 ? K - 1 : 0) * c_full;
+        total = K > 0 ? n_first + c_last : 0;
+    }
+    // Item i < total: the unit it needs staged by every rank, the kept output
+    // it is stored into (qlist index; -1 = every output) and its vector.
+    RR_HD void item(int64_t i, int &unit, int &m, int64_t &v) const
+    {
+        int k;
+        int64_t j;
+        if (i < n_first) {
+            k = (int)(i / c_full);
+            j = i - (int64_t)k * c_full;
+        } else {
+            k = K - 1;
+            j = i - n_first;
+        }
+        const int64_t ps = own0 + ((int64_t)b + (int64_t)k * B) * P;
+        if (twoshot) {
+            unit = k * nranges + r;
+            m = -1;
+            v = ps + j;
+        } else {
+            const int64_t L = k == K - 1 ? L_last : P;
+            const int64_t pos = split_point((int64_t)nout * L, W, r) + j;
+            m = (int)(pos / L);
+            unit = k;
+            v = ps + pos - (int64_t)m * L;
+        }
+    }
+};
+
 // ---------------------------------------------------------------- launchers
 // Implemented in rr_allreduce.cu / rr_allgather.cu.  Each returns the kernel
 // to launch for the given element type and world size, with its block size

@@ -65,6 +65,92 @@ int main()
             }
         }
     }
+    // Staged copy_mode kernel: every output vector is reduced exactly once,
+    // by a block of index b after every rank's block b has published the unit
+    // that staged it; a block's units stay below 2^kRoundBits.
+    struct Case {
+        int64_t n;
+        int W, B;
+        int64_t opt;
+    };
+    std::vector<Case> cases;
+    const int64_t ssizes[] = {0, 1, 15, 16, 17, 255, 256, 257, 1023, 1024, 1025, 4096, 12345, 65543};
+    const int sWs[] = {1, 2, 3, 5, 8, 16};
+    const int sBs[] = {1, 2, 3, 7, 19};
+    const int64_t opts[] = {0, 256, 4096, 65536};
+    for (int64_t n : ssizes)
+        for (int W : sWs)
+            for (int B : sBs)
+                for (int64_t o : opts) cases.push_back({n, W, B, o});
+    cases.push_back({(1 << 21) / 8 + 3, 8, 19, 0});   // W=8, 2^21 bf16 + a few vectors
+    cases.push_back({(1 << 21) + 7, 8, 19, 0});
+    cases.push_back({(int64_t)40000000, 2, 1, 256});  // P grows: one block, 16-byte option
+    for (const Case &cs : cases) {
+        const int64_t n = cs.n;
+        for (int twoshot = 0; twoshot < 2; ++twoshot) {
+            const int W = cs.W, B = cs.B, nr = twoshot ? W : 1;
+            std::vector<int64_t> r0(nr), r1(nr);
+            for (int j = 0; j < nr; ++j) {
+                if (twoshot) owned_segment(n, W, j, r0[j], r1[j]);
+                else { r0[j] = 0; r1[j] = n; }
+            }
+            const int64_t P = staged_piece_vectors(cs.opt, r1[0] - r0[0], nr, B);
+            CHECK(P % kGranuleVec == 0 && P >= kGranuleVec, "staged P=%lld not in granules\n", (long long)P);
+            if (n > 4000000) continue;  // the size only checks that P grows
+            // producer: the block and unit that stage each vector (same on every rank)
+            std::vector<int> sb(n, -1), su(n, -1);
+            for (int b = 0; b < B; ++b) {
+                const int units = staged_rounds(r1[0] - r0[0], P, B, b) * nr;
+                CHECK(units < (1 << kRoundBits), "staged units %d\n", units);
+                for (int u = 0; u < units; ++u) {
+                    int64_t ps, pe;
+                    staged_piece(r0[u % nr], r1[u % nr], P, B, b, u / nr, ps, pe);
+                    for (int64_t v = ps; v < pe; ++v) {
+                        CHECK(sb[v] < 0, "vector %lld staged twice\n", (long long)v);
+                        sb[v] = b;
+                        su[v] = u;
+                    }
+                }
+            }
+            for (int64_t v = 0; v < n; ++v) CHECK(sb[v] >= 0, "vector %lld never staged n=%lld W=%d B=%d\n", (long long)v, (long long)n, W, B);
+            const int nouts[] = {1, W};
+            for (int nout : nouts) {
+                if (twoshot && nout != W) continue;
+                std::vector<int> red((size_t)n * nout, 0);
+                for (int r = 0; r < W; ++r)
+                    for (int b = 0; b < B; ++b) {
+                        StagedItems it;
+                        const int jo = twoshot ? r : 0;
+                        it.init(twoshot != 0, r0[jo], r1[jo], P, B, b, r, W, nout);
+                        int prev_unit = -1;
+                        for (int64_t i = 0; i < it.total; ++i) {
+                            int unit, m;
+                            int64_t v;
+                            it.item(i, unit, m, v);
+                            CHECK(v >= 0 && v < n, "item vector %lld out of range\n", (long long)v);
+                            if (v < 0 || v >= n) continue;
+                            CHECK(unit >= prev_unit, "items not in unit order\n");
+                            prev_unit = unit;
+                            CHECK(sb[v] == b && su[v] <= unit,
+                                  "item reads vector %lld before its unit (block %d unit %d, staged by %d unit %d)\n",
+                                  (long long)v, b, unit, sb[v], su[v]);
+                            if (twoshot) {
+                                CHECK(m == -1 && v >= r0[r] && v < r1[r], "two-shot item outside own segment\n");
+                                red[v]++;
+                            } else {
+                                CHECK(m >= 0 && m < nout, "output index %d\n", m);
+                                if (m >= 0 && m < nout) red[(size_t)m * n + v]++;
+                            }
+                        }
+                    }
+                const int64_t expect = twoshot ? n : (int64_t)nout * n;
+                for (int64_t x = 0; x < expect; ++x)
+                    CHECK(red[x] == 1, "staged %s n=%lld W=%d B=%d P=%lld nout=%d: item %lld reduced %d times\n",
+                          twoshot ? "two-shot" : "one-shot", (long long)n, W, B, (long long)P, nout, (long long)x, red[x]);
+            }
+        }
+    }
+
     if (failures) {
         std::printf("%d failures\n", failures);
         return 1;
