@@ -14,6 +14,6 @@ from ._binding import (  # noqa: F401
     RR_ERR_TOO_MANY_BLOCKS, RR_ERR_UNSUPPORTED_DTYPE, RR_ERR_WRONG_DEVICE, RR_FP16, RR_FP32, RR_INT32,
     RR_MAX_SPLITS, RR_MAX_WORLD, RR_OK, RRError, SignalPad, bound_call, dtype_code, lib,
     pointer_array, rr_allgather, rr_allgather_list, rr_allgather_param_contiguous, rr_allreduce_oneshot,
-    rr_allreduce_twoshot, rr_signal_pad_create, rr_signal_pad_destroy, rr_signal_pad_status,
-    stream_handle,
+    rr_allreduce_oneshot_noalloc, rr_allreduce_oneshot_noalloc_status, rr_allreduce_twoshot,
+    rr_signal_pad_create, rr_signal_pad_destroy, rr_signal_pad_status, stream_handle,
 )

@@ -67,6 +67,8 @@ def lib():
             "rr_allgather": [_PP, _PP, i32, i64, i32, _vp, _vp],
             "rr_allgather_param_contiguous": [_PP, _PP, i32, ctypes.POINTER(i64), i32, i32, _vp, _vp],
             "rr_allgather_list": [_PP, _PP, i32, i64, i32, _vp, _vp],
+            "rr_allreduce_oneshot_noalloc": [_PP, _PP, _PP, i32, i64, i32, i32, _vp],
+            "rr_allreduce_oneshot_noalloc_status": [_vp],
         }
         for name, args in sig.items():
             f = getattr(l, name)
@@ -198,6 +200,20 @@ def rr_allreduce_twoshot(inputs, rank_bufs, outputs, world_size, numel, dtype, c
     _check(lib().rr_allreduce_twoshot(ins, pointer_array(rank_bufs), pointer_array(outputs),
                                       world_size, numel, dtype_code(dtype), int(bool(copy_mode)),
                                       _pad_handle(pad), stream_handle(stream)))
+
+
+def rr_allreduce_oneshot_noalloc(inputs, rank_bufs, outputs, world_size, numel, dtype, copy_mode,
+                                 stream=None):
+    """The one-shot allreduce without a pad (the library's static signal array)."""
+    ins = pointer_array(inputs) if inputs is not None else None
+    _check(lib().rr_allreduce_oneshot_noalloc(ins, pointer_array(rank_bufs), pointer_array(outputs),
+                                              world_size, numel, dtype_code(dtype),
+                                              int(bool(copy_mode)), stream_handle(stream)))
+
+
+def rr_allreduce_oneshot_noalloc_status(stream=None):
+    """Synchronise the stream; raise RRError if the last allocation-free call timed out."""
+    _check(lib().rr_allreduce_oneshot_noalloc_status(stream_handle(stream)))
 
 
 def rr_allgather(rank_bufs, outputs, world_size, numel_per_rank, dtype, pad, stream=None):

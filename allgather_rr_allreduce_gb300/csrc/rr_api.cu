@@ -130,14 +130,20 @@ int sm_count(int dev)
     return it == g_sms.end() ? 0 : it->second;
 }
 
-// Blocks per rank: enough that each block moves about kBytesPerBlock, no
+// Blocks per rank: enough that each block moves about `per_block` bytes, no
 // more than the pad allows, and few enough that all W*B blocks are resident
 // at once (the ranks' blocks wait on each other, so every one of them must
 // be running).  A fixed count set on the pad overrides the first rule.
+// Gathers: 32 KiB per block.  Reductions: 96 KiB per block (their
+// small-message latency, W=8, graph-replayed, was lowest with about one block
+// per 16 KiB per rank for the one-shot with every output kept and one per
+// 32 KiB for the two-shot: each block added to a barrier costs more than the
+// bytes it takes over).  Large messages reach the residency cap either way.
 constexpr int64_t kBytesPerBlock = 32 * 1024;
+constexpr int64_t kReduceBytesPerBlock = 96 * 1024;
 
 rr_status plan_blocks(rr_signal_pad *pad, const rr::KernelChoice &k, int W, int64_t total_bytes,
-                      int *B)
+                      int *B, int64_t per_block = kBytesPerBlock)
 {
     int resident = 0;
     rr_status st = resident_blocks(pad->device, k, &resident);
@@ -157,7 +163,7 @@ rr_status plan_blocks(rr_signal_pad *pad, const rr::KernelChoice &k, int W, int6
         const int pref = k.per_sm * sm_count(pad->device) / W;
         if (pref >= 1 && pref < cap) cap = pref;
     }
-    int64_t want = (total_bytes + (int64_t)W * kBytesPerBlock - 1) / ((int64_t)W * kBytesPerBlock);
+    int64_t want = (total_bytes + (int64_t)W * per_block - 1) / ((int64_t)W * per_block);
     if (want < 1) want = 1;
     *B = (int)(want < cap ? want : cap);
     return RR_OK;
@@ -364,7 +370,7 @@ rr_status allreduce_common(bool twoshot, const void *const *inputs, void *const 
                             : (int64_t)nout * bytes * (W + 1);
     if (copy_mode) moved += 2 * (int64_t)W * bytes;
     int B = 0;
-    st = plan_blocks(pad, k, W, moved, &B);
+    st = plan_blocks(pad, k, W, moved, &B, kReduceBytesPerBlock);
     if (st != RR_OK) return st;
 
     rr::ReduceArgs a;
@@ -385,11 +391,17 @@ rr_status allreduce_common(bool twoshot, const void *const *inputs, void *const 
         // chunks split an owned segment
         const int64_t ng = (a.nvec + rr::kGranuleVec - 1) / rr::kGranuleVec;
         const int64_t seg = twoshot ? (ng + W - 1) / W : ng;
-        const int64_t longest = ((seg + B - 1) / B) * rr::kGranuleVec;
-        // Default round sizes keep one round of every block's staged bytes
-        // well inside L2: the two-shot stages W ranges per round.
-        const int64_t pref = twoshot ? ((tma && copy_mode) ? 2048 : 512) : ((tma && copy_mode) ? 16384 : 4096);
-        a.round_vec = round_vectors(pad->round_bytes, pref, longest);
+        if (tma && copy_mode) {
+            // staged kernel: pieces of the message (one-shot) or of every
+            // owner's segment (two-shot), dealt to the rank's blocks in turn
+            const int64_t seglen = seg * rr::kGranuleVec < a.nvec ? seg * rr::kGranuleVec : a.nvec;
+            a.round_vec = rr::staged_piece_vectors(pad->round_bytes, seglen, twoshot ? W : 1, B);
+        } else {
+            const int64_t longest = ((seg + B - 1) / B) * rr::kGranuleVec;
+            // Default round sizes keep one round of every block's bytes well
+            // inside L2: the two-shot moves W ranges per round.
+            a.round_vec = round_vectors(pad->round_bytes, twoshot ? 512 : 4096, longest);
+        }
     }
     a.iters = iterate ? pad->iters : 1;
     a.skew_ns = iterate ? pad->skew_ns : 0u;
@@ -855,6 +867,28 @@ std::map<int, NoAllocDevice> g_noalloc;
 static __device__ __align__(256) uint32_t
     noalloc_scratch[kNoAllocFlagWords + kNoAllocRoundWords + rr::kStatusWords];
 
+namespace {
+
+// The record of device `dev` (caller holds g_noalloc_mu).  First use on a
+// device: look up the array's device address with this device current (the
+// host-side name is not a device address).  A cudaDeviceReset of the device
+// voids the address kept here; this library does not support calls on a
+// device after it was reset.
+rr_status noalloc_device(int dev, NoAllocDevice **out)
+{
+    auto it = g_noalloc.find(dev);
+    if (it == g_noalloc.end()) {
+        void *addr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&addr, noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(noalloc_scratch)");
+        it = g_noalloc.emplace(dev, NoAllocDevice{static_cast<uint32_t *>(addr), 0u}).first;
+    }
+    *out = &it->second;
+    return RR_OK;
+}
+
+}  // namespace
+
 extern "C" rr_status rr_allreduce_oneshot_noalloc(const void *const *inputs, void *const *rank_bufs,
                                                   void *const *outputs, int world_size, int64_t numel,
                                                   rr_dtype dtype, int copy_mode, cudaStream_t stream)
@@ -902,26 +936,33 @@ extern "C" rr_status rr_allreduce_oneshot_noalloc(const void *const *inputs, voi
     }
     if (numel == 0) return ok();
 
+    // Each call takes its generation from a host counter and passes it as a
+    // kernel argument; a launch captured into a CUDA graph would replay with
+    // the same generation, so flags from the previous replay would already
+    // satisfy its waits.  Refuse the call while the stream is capturing.
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &capture);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    if (capture != cudaStreamCaptureStatusNone)
+        return fail(RR_ERR_INVALID_ARG,
+                    "the stream is being captured: the allocation-free one-shot takes a new generation from a "
+                    "host counter per call, which a graph replay would repeat; use rr_allreduce_oneshot with a "
+                    "pad in device-generation mode inside graphs");
+
     int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
+    e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     uint32_t *scratch = nullptr;
     uint64_t gen = 0;
     {
-        // First call on this device: look up the array's device address with
-        // this device current (the host-side name is not a device address).
         std::lock_guard<std::mutex> lock(g_noalloc_mu);
-        auto it = g_noalloc.find(dev);
-        if (it == g_noalloc.end()) {
-            void *addr = nullptr;
-            e = cudaGetSymbolAddress(&addr, noalloc_scratch);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(noalloc_scratch)");
-            it = g_noalloc.emplace(dev, NoAllocDevice{static_cast<uint32_t *>(addr), 0u}).first;
-        }
-        it->second.gen += 1;
-        if ((uint32_t)it->second.gen == 0) it->second.gen += 2;
-        scratch = it->second.scratch;
-        gen = it->second.gen;
+        NoAllocDevice *d = nullptr;
+        rr_status st = noalloc_device(dev, &d);
+        if (st != RR_OK) return st;
+        d->gen += 1;
+        if ((uint32_t)d->gen == 0) d->gen += 2;
+        scratch = d->scratch;
+        gen = d->gen;
     }
 
     const rr::KernelChoice k = rr::oneshot_kernel_for(dtype, W, copy_mode != 0);
@@ -932,7 +973,7 @@ extern "C" rr_status rr_allreduce_oneshot_noalloc(const void *const *inputs, voi
     if (cap > kNoAllocMaxBlocks) cap = kNoAllocMaxBlocks;
     if (cap < 1) return fail(RR_ERR_TOO_MANY_BLOCKS, "%d ranks do not fit on the device at once", W);
     int64_t moved = (int64_t)nout * bytes * (W + 1) + (copy_mode ? 2 * (int64_t)W * bytes : 0);
-    int64_t want = (moved + (int64_t)W * kBytesPerBlock - 1) / ((int64_t)W * kBytesPerBlock);
+    int64_t want = (moved + (int64_t)W * kReduceBytesPerBlock - 1) / ((int64_t)W * kReduceBytesPerBlock);
     const int B = (int)(want < 1 ? 1 : (want < cap ? want : cap));
 
     // The array keeps the last call's words: the status words must start at
@@ -985,4 +1026,30 @@ extern "C" rr_status rr_allreduce_oneshot_noalloc(const void *const *inputs, voi
     e = cudaLaunchKernelExC(&cfg, k.fn, params);
     if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC");
     return ok();
+}
+
+extern "C" rr_status rr_allreduce_oneshot_noalloc_status(cudaStream_t stream)
+{
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int dev = -1;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    uint32_t *status_words = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        auto it = g_noalloc.find(dev);
+        if (it == g_noalloc.end()) return ok();  // no call on this device yet
+        status_words = it->second.scratch + kNoAllocFlagWords + kNoAllocRoundWords;
+    }
+    uint32_t words[rr::kStatusWords];
+    e = cudaMemcpy(words, status_words, sizeof words, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status words)");
+    if (words[rr::kStErr] == 0 && words[rr::kStAbort] == 0) return ok();
+    e = cudaMemsetAsync(status_words, 0, sizeof words, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the status words");
+    const rr_status dev_status = words[rr::kStErr] ? (rr_status)words[rr::kStErr] : RR_ERR_TIMEOUT;
+    return fail(dev_status, "barrier %u timed out: waiting rank %u, block %u, generation %u", words[rr::kStBarrier],
+                words[rr::kStRank], words[rr::kStBlock], words[rr::kStGen]);
 }

@@ -89,9 +89,12 @@ typedef enum {
                                    barrier and ignore a pending timeout on the pad */
     RR_OPT_INJECT_SKIP = 3,     /* fault injection: -1 = off; else rank*4 + barrier: that rank
                                    never emits that barrier's flags, so peers time out */
-    RR_OPT_ROUND_BYTES = 4,     /* bytes per rank per round of a pipelined chunk (copy_mode
-                                   staging, two-shot); 0 = automatic (64 KiB one-shot,
-                                   32 KiB two-shot) */
+    RR_OPT_ROUND_BYTES = 4,     /* bytes per rank per round of a pipelined chunk; 0 = automatic.
+                                   Bulk-copy copy_mode kernels: the piece of each range staged
+                                   and published as one unit (automatic 16 KiB).  Load/store
+                                   kernels: the round of a block's chunk (automatic 64 KiB
+                                   one-shot, 8 KiB per range two-shot).  Grown where a block
+                                   would pass 65535 rounds */
     RR_OPT_REDUCE_ENGINE = 5,   /* 0 = automatic (bulk copies for copy_mode, loads/stores
                                    otherwise), 1 = 128-bit loads/stores, 2 = bulk-copy (TMA)
                                    engine: copy_mode off, the one-shot's loads stream into a
@@ -162,7 +165,12 @@ typedef struct rr_signal_pad rr_signal_pad; /* opaque, owned by the library */
 rr_status rr_signal_pad_create(int world_size, int max_blocks_per_rank, uint64_t timeout_ns,
                                rr_signal_pad **out);
 
-/* Free the pad's device memory (synchronises the device first). NULL is a no-op. */
+/*
+ * Free the pad's device memory (synchronises the device first).  NULL is a
+ * no-op.  No passage on the pages covers the pad's lifecycle: the sglang
+ * discussion's signal arrays are set up once per communicator and live as
+ * long as it does, which is what create / destroy bracket here.
+ */
 rr_status rr_signal_pad_destroy(rr_signal_pad *pad);
 
 /*
@@ -171,6 +179,10 @@ rr_status rr_signal_pad_destroy(rr_signal_pad *pad);
  * Reading the status clears it.  While a timeout is pending, every later call
  * on the pad exits at its first barrier without writing outputs.
  * rr_signal_pad_timeout_info gives where the first timeout happened.
+ * No passage on the pages covers it: their barrier loops spin without a
+ * bound ("Question and suggestions about custom allreduce", sglang discussion
+ * 2918, multi_gpu_barrier / block_barrier), and this library bounds every
+ * wait and reports the failure here instead of hanging the GPU.
  */
 rr_status rr_signal_pad_status(rr_signal_pad *pad, cudaStream_t stream);
 
@@ -337,16 +349,35 @@ rr_status rr_allgather_list(const void *const *rank_bufs, void *const *output_li
  * with a message naming the limit) and at most 32 blocks per rank (chosen
  * automatically).  The first call on a device looks up the array's device
  * address with that device current; make that first call before any stream
- * capture.  Every call on a device shares the one array: calls that overlap
- * on the GPU (different streams, or other threads) race on it, so serialise
- * them.  Each call clears the array's status words on `stream` before its
- * kernel; a barrier timeout is not reported back (the kernel stops early and
- * its outputs are incomplete), which happens only if the GPU cannot keep all
- * ranks' blocks running at once for 2 s.
+ * capture.  A call made while `stream` is being captured into a CUDA graph
+ * returns RR_ERR_INVALID_ARG: each call takes a new flag generation from a
+ * host counter, and a replayed launch would repeat it.  After a
+ * cudaDeviceReset of a device, calls on it are not supported (the address
+ * looked up by the first call is void).  Every call on a device shares the
+ * one array: calls that overlap on the GPU (different streams, or other
+ * threads) race on it, so serialise them.  Each call clears the array's
+ * status words on `stream` before its kernel.  A barrier that times out (only
+ * if the GPU cannot keep all ranks' blocks running at once for 2 s) stops the
+ * kernel early with incomplete outputs and is recorded in those words: read
+ * it with rr_allreduce_oneshot_noalloc_status.
  */
 rr_status rr_allreduce_oneshot_noalloc(const void *const *inputs, void *const *rank_bufs,
                                        void *const *outputs, int world_size, int64_t numel,
                                        rr_dtype dtype, int copy_mode, cudaStream_t stream);
+
+/*
+ * rr_allreduce_oneshot_noalloc_status -- the device status of the allocation-
+ * free one-shot on the current device, read without allocating.
+ *
+ * The pages have no counterpart (it belongs to rr_allreduce_oneshot_noalloc).
+ * Synchronises `stream`, copies the status words of the static array into a
+ * local host array and returns RR_OK, or RR_ERR_TIMEOUT (rr_last_error says
+ * which barrier, rank, block and generation) if a barrier wait of the last
+ * call enqueued before the read ran out of time; reading clears it.  Returns
+ * RR_OK when no call has been made on the device.  Calls no cudaMalloc,
+ * cudaFree or allocating routine.
+ */
+rr_status rr_allreduce_oneshot_noalloc_status(cudaStream_t stream);
 
 /* Name of a status code (static string). */
 const char *rr_status_string(rr_status s);

@@ -68,13 +68,24 @@ int main(void)
               "rr_allreduce_twoshot"))
         return 1;
     if (check(rr_signal_pad_status(pad, 0), "status after two-shot")) return 1;
-    for (int pass = 0; pass < 2; ++pass) {
+    static const char *const names[3] = {"two-shot", "one-shot", "allocation-free one-shot"};
+    for (int pass = 0; pass < 3; ++pass) {
         if (pass == 1) {
             if ((e = cudaMemset(outs[W - 1], 0xff, N * sizeof(float))) != cudaSuccess) return fail_cuda(e, "cudaMemset");
             if (check(rr_allreduce_oneshot(no_inputs, (void *const *)bufs, (void *const *)outs, W, N, RR_FP32, 0, pad, 0),
                       "rr_allreduce_oneshot"))
                 return 1;
             if (check(rr_signal_pad_status(pad, 0), "status after one-shot")) return 1;
+        }
+        if (pass == 2) {
+            /* no pad: the library's static signal array */
+            for (int q = 0; q < W; ++q)
+                if ((e = cudaMemset(outs[q], 0xff, N * sizeof(float))) != cudaSuccess) return fail_cuda(e, "cudaMemset");
+            if (check(rr_allreduce_oneshot_noalloc(no_inputs, (void *const *)bufs, (void *const *)outs, W, N, RR_FP32,
+                                                   0, 0),
+                      "rr_allreduce_oneshot_noalloc"))
+                return 1;
+            if (check(rr_allreduce_oneshot_noalloc_status(0), "status after the allocation-free one-shot")) return 1;
         }
         for (int q = 0; q < W; ++q) {
             if ((e = cudaMemcpy(host_out, outs[q], N * sizeof(float), cudaMemcpyDeviceToHost)) != cudaSuccess)
@@ -83,8 +94,7 @@ int main(void)
                 float want = 0.0f;
                 for (int r = 0; r < W; ++r) want += host_in[r][i];
                 if (host_out[i] != want) {
-                    fprintf(stderr, "%s output %d element %d: %g, want %g\n", pass ? "one-shot" : "two-shot", q, i,
-                            host_out[i], want);
+                    fprintf(stderr, "%s output %d element %d: %g, want %g\n", names[pass], q, i, host_out[i], want);
                     return 1;
                 }
             }
