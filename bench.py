@@ -523,48 +523,61 @@ def ag_sweep(rr, stream):
 
 
 def fsdp_28_layers(rr, stream):
-    """28 param-contiguous allgathers back to back, one per layer, on distinct
-    buffers (about 13 GB in, 13 GB out), rank 0's output."""
+    """28 param-contiguous allgathers back to back, one per layer, rank 0's
+    output.  All layers' shards sit in one tensor and all outputs in another
+    (about 13 GB each), so where the buffers land does not depend on what the
+    process allocated before."""
     cfg = workloads.FSDP_LAYER
+    L = cfg["layers"]
     splits = workloads.shard_sizes(workloads.FSDP_LAYER_PARAMS, W)
     S = sum(splits)
     pad = rr.rr_signal_pad_create(W)
     g = torch.Generator(device="cuda").manual_seed(cfg["seed_base"])
     import ctypes
     sp = (ctypes.c_int64 * len(splits))(*splits)
-    calls, keep = [], []
-    for _ in range(cfg["layers"]):
-        x = (torch.randn((W, S), generator=g, device="cuda") * cfg["sigma"]).to(torch.bfloat16)
-        y = torch.empty(W * S, dtype=torch.bfloat16, device="cuda")
-        keep.append((x, y))
-        calls.append(rr.bound_call("rr_allgather_param_contiguous", [x[r].data_ptr() for r in range(W)],
-                                   [y.data_ptr()] + [None] * (W - 1), W, sp, len(splits), rr.RR_BF16,
-                                   pad, stream.cuda_stream))
-    def one_pass():
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for c in calls:
+    X = torch.empty((L, W, S), dtype=torch.bfloat16, device="cuda")
+    for l in range(L):
+        X[l].copy_((torch.randn((W, S), generator=g, device="cuda") * cfg["sigma"]).to(torch.bfloat16))
+    Y = torch.empty((L, W * S), dtype=torch.bfloat16, device="cuda")
+    calls = [rr.bound_call("rr_allgather_param_contiguous", [X[l, r].data_ptr() for r in range(W)],
+                           [Y[l].data_ptr()] + [None] * (W - 1), W, sp, len(splits), rr.RR_BF16,
+                           pad, stream.cuda_stream) for l in range(L)]
+
+    def one_pass(per_layer=False):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(L + 1)]
+        evs[0].record(stream)
+        for i, c in enumerate(calls):
             c()
-        e1.record(stream)
-        e1.synchronize()
-        return e0.elapsed_time(e1)
+            if per_layer or i == L - 1:
+                evs[i + 1].record(stream)
+        evs[-1].synchronize()
+        per = [1000 * evs[i].elapsed_time(evs[i + 1]) for i in range(L)] if per_layer else None
+        return evs[0].elapsed_time(evs[-1]), per
 
     # A training step gathers the same persistent buffers every step: the
     # figure is the steady state after 8 untimed passes; the first pass over
-    # the freshly made layers is reported beside it.
-    first = one_pass()
+    # the fresh layers (whose first call also touches the output memory for
+    # the first time) is reported beside it.
+    first, first_per = one_pass(True)
     for _ in range(8):
         one_pass()
-    ms = min(one_pass() for _ in range(4))
+    ms = min(one_pass()[0] for _ in range(4))
+    _, steady_per = one_pass(True)
     pad.status(stream)
     pad.close()
-    total = cfg["layers"] * 2 * W * S * EB
+    total = L * 2 * W * S * EB
+    del X, Y
+    torch.cuda.empty_cache()
     return {"ms": round(ms, 4), "GBps": round(total / ms / 1e6, 1), "bytes": total,
             "pct_of_8TBps": round(100 * total / ms / 1e6 / NOMINAL_HBM_GBS, 2),
-            "us_per_layer": round(1000 * ms / cfg["layers"], 2),
-            "first_pass_us_per_layer": round(1000 * first / cfg["layers"], 2),
-            "how": "steady state: best of 4 passes after 8 untimed passes over the 28 layers"}
+            "us_per_layer": round(1000 * ms / L, 2),
+            "first_pass_us_per_layer": round(1000 * first / L, 2),
+            "first_pass_first_layer_us": round(first_per[0], 1),
+            "first_pass_other_layers_us_median": round(statistics.median(first_per[1:]), 1),
+            "steady_layer_us_min_median_max": [round(min(steady_per), 1), round(statistics.median(steady_per), 1),
+                                               round(max(steady_per), 1)],
+            "how": "steady state: best of 4 passes after 8 untimed passes over the 28 layers; per-layer "
+                   "figures from one more pass with an event pair around every layer"}
 
 
 def overlap_gemm(rr, stream, n_ag=40, mkn=8192):

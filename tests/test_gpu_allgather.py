@@ -176,7 +176,8 @@ def test_allgather_size_sweep(rr, dtype):
     """W=8, 1 KiB .. 512 MiB per rank, random bits.  Up to 64 MiB per rank
     the whole output is compared with the oracle on the host; above, on the
     device, with the property every size obeys: output slice r is rank r's
-    shard (the output crosses 2^32 bytes at 512 MiB per rank)."""
+    shard (at 512 MiB per rank the output is exactly 2^32 bytes, so its last
+    byte offset is 2^32 - 1; test_gathers_past_4_gib goes beyond)."""
     W = 8
     eb = workloads.ELEM_BYTES[dtype]
     pad = pad_for(rr, W)
@@ -205,6 +206,73 @@ def test_allgather_size_sweep(rr, dtype):
             assert torch.equal(out.view(W, n), shards), f"{nbytes} B per rank"
             del shards, out
             torch.cuda.empty_cache()
+
+
+# Byte offsets of 2^31 and 2^32 and more: a gather whose output passes 4 GiB
+# ("ccl: hierarchical cross-node AllGather (intra-node SDMA + inter-node RDMA)
+# #441": its large-profile commit probes u32 byte-offset overflow with a
+# gathered int32 output past 2^31 bytes).  576 MiB per rank at W=8: a 4.5 GiB
+# output.
+BIG_BYTES = 576 << 20
+WINDOWS = (1 << 31, 1 << 32)
+
+
+def _host_windows(t_bytes, centers, half=8192):
+    """Bytes [c - half, c + half) of a device uint8 view, for each center c."""
+    return [t_bytes[c - half:c + half].cpu().numpy() for c in centers]
+
+
+@pytest.mark.parametrize("kind", ["rank_major", "param_contiguous"])
+def test_gathers_past_4_gib(rr, kind):
+    """W=8, 576 MiB of random bits per rank, output 4.5 GiB, on every gather
+    engine: the whole output is checked on the device against the layout
+    definition, and compared with the oracle on the host (the whole output
+    for the default engine, 16 KiB windows around byte offsets 2^31 and 2^32
+    and the last 16 KiB for every engine).  The param-contiguous table puts a
+    piece across 2^32 bytes and the last two params past it."""
+    W, dtype = 8, "int32"
+    n = BIG_BYTES // 4
+    gen = torch.Generator(device="cuda").manual_seed(4321)
+    shards = torch.randint(-(1 << 31), (1 << 31) - 1, (W, n), dtype=torch.int32, device="cuda", generator=gen)
+    host_in = [shards[r].cpu().numpy() for r in range(W)]
+    if kind == "rank_major":
+        splits = [n]
+        want = oracle.allgather_rank_major_mt(host_in, dtype)
+    else:
+        splits = [n - 1_000_003 - 5, 5, 1_000_003]
+        want = oracle.allgather_param_contiguous_mt(host_in, splits, dtype)
+    want_b = want.view(np.uint8)
+    total = W * n * 4
+    assert total > (1 << 32) + (1 << 20)
+    out = torch.empty(W * n, dtype=torch.int32, device="cuda")
+    pad = pad_for(rr, W)
+    try:
+        for engine in (0, 2, 3):
+            pad.set_option("gather_engine", engine)
+            out.fill_(-1)
+            if kind == "rank_major":
+                rr.rr_allgather([shards[r] for r in range(W)], [out] + [None] * (W - 1), W, n, dtype, pad)
+            else:
+                rr.rr_allgather_param_contiguous([shards[r] for r in range(W)], [out] + [None] * (W - 1), W,
+                                                 splits, dtype, pad)
+            pad.status()
+            # the definition, on the device
+            o = 0
+            for e in splits:
+                got = out[o * W:(o + e) * W].view(W, e)
+                assert torch.equal(got, shards[:, o:o + e]), f"engine {engine}: param at element {o}"
+                o += e
+            # the oracle, on the host
+            ob = out.view(torch.uint8)
+            centers = list(WINDOWS) + [total - 8192]
+            for c, w in zip(centers, _host_windows(ob, centers)):
+                assert np.array_equal(w, want_b[c - 8192:c + 8192]), f"engine {engine}: bytes around {c}"
+            if engine == 0:
+                assert np.array_equal(ob.cpu().numpy(), want_b), "engine 0: whole output against the oracle"
+    finally:
+        pad.set_option("gather_engine", 0)
+    del shards, out
+    torch.cuda.empty_cache()
 
 
 def test_gather_argument_errors(rr):

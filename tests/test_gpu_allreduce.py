@@ -376,7 +376,7 @@ def test_large_workload_full(rr, algo, copy_mode):
 
 @pytest.mark.parametrize("algo", ["oneshot", "twoshot", "twoshot_pull"])
 @pytest.mark.parametrize("copy_mode", [0, 1])
-@pytest.mark.parametrize("kib", [8, 64, 256])
+@pytest.mark.parametrize("kib", [8, 16, 32, 64, 128, 256])
 def test_back_to_back_alternating_inputs(rr, algo, copy_mode, kib):
     """1000 back-to-back calls on one pad (generation parity alternates),
     inputs alternating between two sets, each call into its own outputs: a
@@ -406,10 +406,12 @@ def test_back_to_back_alternating_inputs(rr, algo, copy_mode, kib):
             fn(None, s.ptrs, optrs, W, N, dtype, 0, pad, stream)
     pad.status(stream)
     pad.set_option("twoshot_mode", 0)
-    for i in range(calls):
-        w = wants[i % 2]
-        for r in range(W):
-            assert torch.equal(outs[i, r].view(torch.int16), w.view(torch.int16)), f"call {i} rank {r}"
+    o16 = outs.view(torch.int16)
+    for k in range(2):
+        bad = (o16[k::2] != wants[k].view(torch.int16)).any(dim=2)   # [calls / 2, W]
+        if bad.any():
+            i, r = [int(x) for x in bad.nonzero()[0]]
+            raise AssertionError(f"call {2 * i + k} rank {r} holds the wrong sum")
 
 
 def test_zero_elements_is_a_no_op(rr):
