@@ -522,31 +522,34 @@ def ag_sweep(rr, stream):
     return out
 
 
-def fsdp_28_layers(rr, stream):
+class FsdpLayers:
     """28 param-contiguous allgathers back to back, one per layer, rank 0's
     output.  All layers' shards sit in one tensor and all outputs in another
-    (about 13 GB each), so where the buffers land does not depend on what the
-    process allocated before."""
-    cfg = workloads.FSDP_LAYER
-    L = cfg["layers"]
-    splits = workloads.shard_sizes(workloads.FSDP_LAYER_PARAMS, W)
-    S = sum(splits)
-    pad = rr.rr_signal_pad_create(W)
-    g = torch.Generator(device="cuda").manual_seed(cfg["seed_base"])
-    import ctypes
-    sp = (ctypes.c_int64 * len(splits))(*splits)
-    X = torch.empty((L, W, S), dtype=torch.bfloat16, device="cuda")
-    for l in range(L):
-        X[l].copy_((torch.randn((W, S), generator=g, device="cuda") * cfg["sigma"]).to(torch.bfloat16))
-    Y = torch.empty((L, W * S), dtype=torch.bfloat16, device="cuda")
-    calls = [rr.bound_call("rr_allgather_param_contiguous", [X[l, r].data_ptr() for r in range(W)],
-                           [Y[l].data_ptr()] + [None] * (W - 1), W, sp, len(splits), rr.RR_BF16,
-                           pad, stream.cuda_stream) for l in range(L)]
+    (about 13 GB each)."""
 
-    def one_pass(per_layer=False):
+    def __init__(self, rr, stream):
+        import ctypes
+        cfg = workloads.FSDP_LAYER
+        self.L = cfg["layers"]
+        self.stream = stream
+        self.splits = workloads.shard_sizes(workloads.FSDP_LAYER_PARAMS, W)
+        self.S = sum(self.splits)
+        self.pad = rr.rr_signal_pad_create(W)
+        g = torch.Generator(device="cuda").manual_seed(cfg["seed_base"])
+        self._sp = (ctypes.c_int64 * len(self.splits))(*self.splits)
+        self.X = torch.empty((self.L, W, self.S), dtype=torch.bfloat16, device="cuda")
+        for l in range(self.L):
+            self.X[l].copy_((torch.randn((W, self.S), generator=g, device="cuda") * cfg["sigma"]).to(torch.bfloat16))
+        self.Y = torch.empty((self.L, W * self.S), dtype=torch.bfloat16, device="cuda")
+        self.calls = [rr.bound_call("rr_allgather_param_contiguous", [self.X[l, r].data_ptr() for r in range(W)],
+                                    [self.Y[l].data_ptr()] + [None] * (W - 1), W, self._sp, len(self.splits),
+                                    rr.RR_BF16, self.pad, stream.cuda_stream) for l in range(self.L)]
+
+    def one_pass(self, per_layer=False):
+        L, stream = self.L, self.stream
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(L + 1)]
         evs[0].record(stream)
-        for i, c in enumerate(calls):
+        for i, c in enumerate(self.calls):
             c()
             if per_layer or i == L - 1:
                 evs[i + 1].record(stream)
@@ -554,30 +557,33 @@ def fsdp_28_layers(rr, stream):
         per = [1000 * evs[i].elapsed_time(evs[i + 1]) for i in range(L)] if per_layer else None
         return evs[0].elapsed_time(evs[-1]), per
 
-    # A training step gathers the same persistent buffers every step: the
-    # figure is the steady state after 8 untimed passes; the first pass over
-    # the fresh layers (whose first call also touches the output memory for
-    # the first time) is reported beside it.
-    first, first_per = one_pass(True)
-    for _ in range(8):
-        one_pass()
-    ms = min(one_pass()[0] for _ in range(4))
-    _, steady_per = one_pass(True)
-    pad.status(stream)
-    pad.close()
-    total = L * 2 * W * S * EB
-    del X, Y
-    torch.cuda.empty_cache()
-    return {"ms": round(ms, 4), "GBps": round(total / ms / 1e6, 1), "bytes": total,
-            "pct_of_8TBps": round(100 * total / ms / 1e6 / NOMINAL_HBM_GBS, 2),
-            "us_per_layer": round(1000 * ms / L, 2),
-            "first_pass_us_per_layer": round(1000 * first / L, 2),
-            "first_pass_first_layer_us": round(first_per[0], 1),
-            "first_pass_other_layers_us_median": round(statistics.median(first_per[1:]), 1),
-            "steady_layer_us_min_median_max": [round(min(steady_per), 1), round(statistics.median(steady_per), 1),
-                                               round(max(steady_per), 1)],
-            "how": "steady state: best of 4 passes after 8 untimed passes over the 28 layers; per-layer "
-                   "figures from one more pass with an event pair around every layer"}
+    def measure(self):
+        # A training step gathers the same persistent buffers every step: the
+        # figure is the steady state after 8 untimed passes; the first pass
+        # over the fresh layers is reported beside it.
+        L = self.L
+        first, first_per = self.one_pass(True)
+        for _ in range(8):
+            self.one_pass()
+        ms = min(self.one_pass()[0] for _ in range(4))
+        _, steady_per = self.one_pass(True)
+        self.pad.status(self.stream)
+        total = L * 2 * W * self.S * EB
+        return {"ms": round(ms, 4), "GBps": round(total / ms / 1e6, 1), "bytes": total,
+                "pct_of_8TBps": round(100 * total / ms / 1e6 / NOMINAL_HBM_GBS, 2),
+                "us_per_layer": round(1000 * ms / L, 2),
+                "first_pass_us_per_layer": round(1000 * first / L, 2),
+                "first_pass_first_layer_us": round(first_per[0], 1),
+                "first_pass_other_layers_us_median": round(statistics.median(first_per[1:]), 1),
+                "steady_layer_us_min_median_max": [round(min(steady_per), 1), round(statistics.median(steady_per), 1),
+                                                   round(max(steady_per), 1)],
+                "how": "steady state: best of 4 passes after 8 untimed passes over the 28 layers; per-layer "
+                       "figures from one more pass with an event pair around every layer"}
+
+    def close(self):
+        self.pad.close()
+        del self.X, self.Y, self.calls
+        torch.cuda.empty_cache()
 
 
 def overlap_gemm(rr, stream, n_ag=40, mkn=8192):
@@ -669,6 +675,12 @@ def run_gpu(args, rank, world, local_rank):
     rr_build.build()
     torch.cuda.set_device(local_rank)
     stream = torch.cuda.Stream()
+    # The 28 FSDP layers are the first large allocation of the process, as a
+    # training job allocates its weights before its scratch buffers.  (Layers
+    # allocated after the step's buffers gathered 15 % slower on some GPU
+    # boxes, the first two layers 2.4x slower; `fsdp_28_layers_allocated_late`
+    # below measures that placement too.)
+    fsdp_layers = FsdpLayers(rr, stream) if (rank == 0 and not args.no_extras) else None
     ops = tuple(args.only.split(",")) if args.only else OP_NAMES
     step = Step(rr, stream, seed=workloads.LARGE["seed_base"] + 97 * rank, ops=ops,
                 n=args.numel or N, pc_div=args.pc_div)
@@ -726,12 +738,14 @@ def run_gpu(args, rank, world, local_rank):
     max_ms = max_over_ranks(elapsed_ms, world)
 
     # Extras that need only device memory run before the end-to-end leg (which
-    # adds a second set of step buffers and pinned host copies of both); the
-    # 28-layer gather runs again after it, to show whether that changes it.
+    # adds a second set of step buffers and pinned host copies of both).  A
+    # second set of 28 layers, allocated after everything else, is timed at
+    # the end.
     early = {}
     if rank == 0 and not args.no_extras:
         early["ops_alone"] = ops_alone(step)
-        early["fsdp_28_layers"] = fsdp_28_layers(rr, stream)
+        early["fsdp_28_layers"] = fsdp_layers.measure()
+        fsdp_layers.close()
 
     # end to end through the public API: host inputs in, host outputs out
     e2e_steps = max(2, min(args.steps, 6))
@@ -792,7 +806,9 @@ def run_gpu(args, rank, world, local_rank):
 
     extras = dict(early)
     if not args.no_extras:
-        extras["fsdp_28_layers_after_e2e"] = fsdp_28_layers(rr, stream)
+        late = FsdpLayers(rr, stream)
+        extras["fsdp_28_layers_allocated_late"] = late.measure()
+        late.close()
         extras["latency_us"] = latency_sweep(rr, stream)
         extras["small_config"] = small_config_latency(rr, stream)
         extras["allgather_sweep"] = ag_sweep(rr, stream)
