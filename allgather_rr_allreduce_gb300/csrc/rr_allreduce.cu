@@ -629,12 +629,14 @@ __global__ void __launch_bounds__(kRtThreads, 1) oneshot_tma_kernel(const __grid
 // items in unit order (one-shot: the (output, vector) pairs of each piece
 // that fall to this rank's block b, see reduce_share; two-shot: the vectors of
 // the piece of the rank's own segment, each reduced once and stored into
-// every output).  Warp w takes items [32g, 32g + 32) for g = w, w + C, ...
-// (several such groups per pass, to keep 8 or 16 loads in flight per thread);
-// before a pass it reads the poller's count until it covers the pass's last
-// unit.  A unit is consumed a few microseconds after it is staged, while
-// its bytes are still in L2, and the last one leaves only one piece to
-// reduce after the staging ends.  The consumers never poll global flags
+// every output).  Items go in groups of 32, U adjacent groups per warp and
+// pass (U = 2 one-shot, 1 two-shot: 16 or 8 loads in flight per thread): warp
+// w's passes take groups wU .. wU + U - 1, then those CU further on, so one
+// pass needs at most two adjacent units (groups 3C apart waited for the later
+// unit: 104 against 103 us one-shot).  Before a pass the warp reads the
+// poller's count until it covers the pass's last unit.  A unit is consumed
+// about a microsecond after it is staged, while its bytes are still in L2,
+// and the last one leaves only one piece to reduce after the staging ends.  The consumers never poll global flags
 // themselves: a GPU-scope acquire would first wait for their own output
 // stores still in flight.
 // The ragged tail is staged by the consumers before the roles split, so the
@@ -655,9 +657,12 @@ struct SwShape {
     static constexpr int kThreads = kConsumers + 96;
 };
 constexpr int kSwStages = 12;
-constexpr int kSwAhead = 4;          // loads in flight ahead of the store being issued
+// Three loads ahead of the store measured best (W=8 x 32 MiB bf16, one-shot /
+// two-shot us): 2 ahead 118 / 158, 3 ahead 105 / 143, 4 ahead 106 / 147; a
+// landing window of 1 group against 2: 104 / 143 against 105 / 143.
+constexpr int kSwAhead = 3;          // loads in flight ahead of the store being issued
 constexpr int kSwReading = 6;        // store groups allowed to be still reading shared memory
-constexpr int kSwLanding = 2;        // store groups allowed to be still landing in global memory
+constexpr int kSwLanding = 1;        // store groups allowed to be still landing in global memory
 constexpr int kSwUnitRing = 32;      // units of the last kSwUnitRing tiles are remembered
 constexpr int kSwTileBytes = 16384;
 constexpr int kSwSmem = kSwStages * kSwTileBytes;  // 192 KiB
@@ -887,13 +892,13 @@ __device__ __forceinline__ void staged_kernel_body(const ReduceArgs &a, const Si
             }
         };
         bool ok = true;
-        for (int64_t g0 = warp; ok && g0 * 32 < total; g0 += (int64_t)kSwConsumerWarps * UG) {
+        for (int64_t g0 = (int64_t)warp * UG; ok && g0 * 32 < total; g0 += (int64_t)kSwConsumerWarps * UG) {
             uint4 *dst[UG];
             int64_t vv[UG];
             int need = -1;
 #pragma unroll
             for (int u = 0; u < UG; ++u) {
-                const int64_t i = (g0 + (int64_t)u * kSwConsumerWarps) * 32 + lane;
+                const int64_t i = (g0 + u) * 32 + lane;
                 dst[u] = nullptr;
                 vv[u] = 0;
                 if (i < total) {
@@ -911,7 +916,7 @@ __device__ __forceinline__ void staged_kernel_body(const ReduceArgs &a, const Si
             uint4 x[UG][WMAX];
 #pragma unroll
             for (int u = 0; u < UG; ++u) {
-                const int64_t i = (g0 + (int64_t)u * kSwConsumerWarps) * 32 + lane;
+                const int64_t i = (g0 + u) * 32 + lane;
                 if (i < total) {
 #pragma unroll
                     for (int c = 0; c < WMAX; ++c)
@@ -920,7 +925,7 @@ __device__ __forceinline__ void staged_kernel_body(const ReduceArgs &a, const Si
             }
 #pragma unroll
             for (int u = 0; u < UG; ++u) {
-                const int64_t i = (g0 + (int64_t)u * kSwConsumerWarps) * 32 + lane;
+                const int64_t i = (g0 + u) * 32 + lane;
                 if (i < total) {
                     const uint4 y = combine<Op, WMAX>(x[u], W);
                     if constexpr (kTwoShot) {

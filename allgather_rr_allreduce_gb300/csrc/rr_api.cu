@@ -357,8 +357,9 @@ rr_status allreduce_common(bool twoshot, const void *const *inputs, void *const 
     const bool push = pad->twoshot_mode != 1;
     // bulk-copy engine: one-shot loads (copy_mode off), or staging by a
     // producer warp (copy_mode on; for the two-shot only with the push allgather)
-    // automatic: bulk-copy staging for copy_mode (measured faster: 130 vs 138 us
-    // one-shot, 172 vs 175 us two-shot at W=8 x 32 MiB), loads/stores otherwise
+    // automatic: bulk-copy staging for copy_mode (measured faster than the
+    // load/store kernels: 105 vs 135 us one-shot, 144 vs 176 us two-shot at
+    // W=8 x 32 MiB bf16), loads/stores otherwise
     const bool tma = copy_mode ? (pad->reduce_engine != 1 && (!twoshot || push))
                                : (!twoshot && pad->reduce_engine == 2);
     const rr::KernelChoice k = iterate ? rr::iter_reduce_kernel_for(twoshot, W, copy_mode != 0)

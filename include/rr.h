@@ -91,7 +91,9 @@ typedef enum {
                                    never emits that barrier's flags, so peers time out */
     RR_OPT_ROUND_BYTES = 4,     /* bytes per rank per round of a pipelined chunk; 0 = automatic.
                                    Bulk-copy copy_mode kernels: the piece of each range staged
-                                   and published as one unit (automatic 16 KiB).  Load/store
+                                   and published as one unit (automatic: at most 16 KiB, cut
+                                   so that every block of a rank gets the same number of
+                                   pieces where granules allow).  Load/store
                                    kernels: the round of a block's chunk (automatic 64 KiB
                                    one-shot, 8 KiB per range two-shot).  Grown where a block
                                    would pass 65535 rounds */

@@ -113,6 +113,23 @@ int main()
                 }
             }
             for (int64_t v = 0; v < n; ++v) CHECK(sb[v] >= 0, "vector %lld never staged n=%lld W=%d B=%d\n", (long long)v, (long long)n, W, B);
+            if (cs.opt == 0 && r1[0] > r0[0]) {
+                // default pieces: no block stages more than its even share of a
+                // range plus a granule per round
+                const int64_t len = r1[0] - r0[0];
+                const int K = staged_rounds(len, P, B, 0);
+                for (int b = 0; b < B; ++b) {
+                    int64_t mine = 0;
+                    for (int k = 0; k < staged_rounds(len, P, B, b); ++k) {
+                        int64_t ps, pe;
+                        staged_piece(r0[0], r1[0], P, B, b, k, ps, pe);
+                        mine += pe - ps;
+                    }
+                    CHECK(mine <= (len + B - 1) / B + (int64_t)K * kGranuleVec,
+                          "block %d stages %lld of %lld vectors over %d blocks (P=%lld)\n", b, (long long)mine,
+                          (long long)len, B, (long long)P);
+                }
+            }
             const int nouts[] = {1, W};
             for (int nout : nouts) {
                 if (twoshot && nout != W) continue;
