@@ -349,9 +349,13 @@ KernelChoice gather_kernel_for(int engine, bool list)
         return KernelChoice{list ? (const void *)gather_kernel_tma<GatherListArgs>
                                  : (const void *)gather_kernel_tma<GatherArgs>,
                             kTmaThreads, kTmaSmem};
+    // Three blocks per SM where four would fit (62 registers): at W=8 the
+    // rank-major gather of 32 MiB per rank takes 88.1-88.4 against 89.3-89.5
+    // us and one FSDP layer 146.1 against 149.6-150.6 us; two per SM take
+    // 96.5 and 164.5 us.
     return KernelChoice{list ? (const void *)gather_kernel_ldst<GatherListArgs>
                              : (const void *)gather_kernel_ldst<GatherArgs>,
-                        kLdstThreads, 0};
+                        kLdstThreads, 0, 3};
 }
 
 }  // namespace rr
