@@ -240,7 +240,7 @@ def test_staged_copy_mode_matches_oracle(rr, algo, dtype, W, N):
         pad.set_option("reduce_engine", 0)
 
 
-@pytest.mark.parametrize("round_bytes", [256, 16384, 1 << 22])
+@pytest.mark.parametrize("round_bytes", [0, 256, 16384, 1 << 22])  # 0: pieces balanced over the blocks
 @pytest.mark.parametrize("blocks", [1, 3, 19])
 @pytest.mark.parametrize("algo", ["oneshot", "twoshot"])
 def test_staged_rounds_and_blocks(rr, round_bytes, blocks, algo):
