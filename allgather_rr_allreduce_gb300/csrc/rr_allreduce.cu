@@ -632,12 +632,13 @@ __global__ void __launch_bounds__(kRtThreads, 1) oneshot_tma_kernel(const __grid
 // every output).  Items go in groups of 32, U adjacent groups per warp and
 // pass (U = 2 one-shot, 1 two-shot: 16 or 8 loads in flight per thread): warp
 // w's passes take groups wU .. wU + U - 1, then those CU further on, so one
-// pass needs at most two adjacent units (groups 3C apart waited for the later
-// unit: 104 against 103 us one-shot).  Before a pass the warp reads the
-// poller's count until it covers the pass's last unit.  A unit is consumed
-// about a microsecond after it is staged, while its bytes are still in L2,
-// and the last one leaves only one piece to reduce after the staging ends.  The consumers never poll global flags
-// themselves: a GPU-scope acquire would first wait for their own output
+// pass needs at most two adjacent units (a warp's groups C apart, three units
+// at W=8, made each pass wait for the later unit: 104 against 103 us
+// one-shot).  Before a pass the warp reads the poller's count until it covers
+// the pass's last unit.  A unit is consumed about a microsecond after it is
+// staged, while its bytes are still in L2, and the last one leaves only one
+// piece to reduce after the staging ends.  The consumers never poll global
+// flags themselves: a GPU-scope acquire would first wait for their own output
 // stores still in flight.
 // The ragged tail is staged by the consumers before the roles split, so the
 // producer's first release covers it.  END barrier over the whole block.

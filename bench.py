@@ -55,12 +55,39 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def code_tokens(text):
+    """C/C++/CUDA source with comments removed and whitespace runs collapsed
+    (string and character literals kept as written), so that editing a
+    comment leaves the hash of the code unchanged."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_hash():
+    """Hash of the kernel sources' code (comments and layout ignored)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "allgather_rr_allreduce_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 

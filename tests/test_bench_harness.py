@@ -71,3 +71,13 @@ def test_reference_arm_prints_one_json_line():
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["value"] > 0
+
+
+def test_source_hash_ignores_comments_and_layout():
+    sys.path.insert(0, ROOT)
+    import bench
+    code = 'int a = 1; // note\n/* block\n comment */\tconst char *s = "x // y /* z */";\nchar q = \'"\';\n'
+    assert bench.code_tokens(code) == 'int a = 1; const char *s = "x // y /* z */"; char q = \'"\';'
+    assert bench.code_tokens("a  =\n\n b; // x") == bench.code_tokens("a = b;")
+    assert bench.code_tokens("a = b;") != bench.code_tokens("a = c;")
+    assert len(bench.source_hash()) == 16
