@@ -38,7 +38,12 @@ namespace rr {
 
 constexpr int kLdstThreads = 256;
 constexpr int kTmaThreads = 128;
-constexpr int kTmaStages = 4;
+// Two blocks per SM, each with a ring of three 16 KiB stages (two loads in
+// flight ahead of the stores being issued): 64 KiB of loads in flight per SM.
+// At W=8 (us, rank-major 32 MiB per rank / one FSDP layer): three blocks of
+// four stages 92.9 / 152.9, two of three 87.3 / 144.2, four of two 89.2 /
+// 146.2, three of two 95.0 / 159.5, one of six or eight 86.1 / 159.7.
+constexpr int kTmaStages = 3;
 constexpr int kTmaChunk = 16384;  // bytes per stage
 constexpr int kTmaSmem = kTmaStages * kTmaChunk;
 
@@ -348,14 +353,14 @@ KernelChoice gather_kernel_for(int engine, bool list)
     if (engine == 2)
         return KernelChoice{list ? (const void *)gather_kernel_tma<GatherListArgs>
                                  : (const void *)gather_kernel_tma<GatherArgs>,
-                            kTmaThreads, kTmaSmem};
-    // Three blocks per SM where four would fit (62 registers): at W=8 the
-    // rank-major gather of 32 MiB per rank takes 88.1-88.4 against 89.3-89.5
-    // us and one FSDP layer 146.1 against 149.6-150.6 us; two per SM take
-    // 96.5 and 164.5 us.
+                            kTmaThreads, kTmaSmem, 2};
+    // As many blocks as fit (four per SM at 62 registers).  Three per SM were
+    // 2-3% faster on buffers allocated early in a process, but 28 FSDP layers
+    // allocated after other large buffers then took 234 us per layer against
+    // 178 with four (the bulk-copy engine: 147 either way).
     return KernelChoice{list ? (const void *)gather_kernel_ldst<GatherListArgs>
                              : (const void *)gather_kernel_ldst<GatherArgs>,
-                        kLdstThreads, 0, 3};
+                        kLdstThreads, 0};
 }
 
 }  // namespace rr

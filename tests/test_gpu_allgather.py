@@ -120,6 +120,43 @@ def test_param_contiguous_fixed_blocks(rr, engine, blocks):
         assert_bitwise(outs.host(q), want)
 
 
+AUTO_CASES = {
+    # (splits per rank in bf16 elements (None = rank-major), numel, engine expected)
+    "rank_major_16MiB": (None, 8 << 20, 2),
+    "rank_major_16MiB_less_16B": (None, (8 << 20) - 8, 1),
+    "param_aligned": ([3 << 20, 8, 5 << 20, 4096], None, 2),
+    "param_split_off_16B": ([3 << 20, 9, 5 << 20, 4096], None, 1),
+    "rank_major_1MiB": (None, 1 << 19, 1),
+}
+
+
+@pytest.mark.parametrize("case", list(AUTO_CASES))
+def test_automatic_engine_choice(rr, case):
+    """The automatic gather engine: bulk copies from 16 MiB per rank up when
+    every split boundary is a multiple of 16 bytes, loads/stores otherwise;
+    the bytes equal the oracle's either way."""
+    splits, numel, expect = AUTO_CASES[case]
+    W, dtype = 8, "bf16"
+    pad = pad_for(rr, W)
+    pad.set_option("gather_engine", 0)
+    n = numel if splits is None else sum(splits)
+    ins = workloads.rank_buffers(W, n, dtype, "bits", seed_base=77)
+    bufs = RankBuffers(W, n, dtype)
+    bufs.fill(ins)
+    outs = GuardedOutputs(W, W * n, dtype, materialise=(0, 6))
+    if splits is None:
+        want = oracle.allgather_rank_major(ins, dtype)
+        rr.rr_allgather(bufs.ptrs, outs.ptrs, W, n, dtype, pad)
+    else:
+        want = oracle.allgather_param_contiguous(ins, splits, dtype)
+        rr.rr_allgather_param_contiguous(bufs.ptrs, outs.ptrs, W, splits, dtype, pad)
+    pad.status()
+    assert pad.get_option("last_engine") == expect
+    for q in (0, 6):
+        assert_bitwise(outs.host(q), want, f"{case} output {q}")
+    outs.check_guards()
+
+
 @pytest.mark.parametrize("engine", list(ENGINES))
 def test_fsdp_layer_full(rr, engine):
     """One transformer layer (hidden 3584 / kv 512 / ffn 18944), W=8, bf16,
