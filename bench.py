@@ -46,6 +46,9 @@ OP_NAMES = ("oneshot_copy_off", "oneshot_copy_on", "twoshot_copy_off", "twoshot_
             "allgather", "allgather_pc")
 
 
+GATHER_ENGINES = ("auto", "ldst", "tma", "copy_engine")  # pad option gather_engine 0..3
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -713,6 +716,7 @@ def run_gpu(args, rank, world, local_rank):
                 n=args.numel or N, pc_div=args.pc_div)
     step.pad.set_option("reduce_engine", ("auto", "ldst", "tma").index(args.reduce_engine))
     step.pad.set_option("twoshot_mode", ("auto", "pull", "push").index(args.twoshot_mode))
+    step.pad.set_option("gather_engine", GATHER_ENGINES.index(args.gather_engine))
     bytes_by_op = step.bytes_by_op()
     step_bytes = sum(bytes_by_op.values())
     torch.cuda.synchronize()
@@ -793,7 +797,7 @@ def run_gpu(args, rank, world, local_rank):
     # sets (the headline e2e)
     step_b = Step(rr, stream, seed=workloads.LARGE["seed_base"] + 97 * rank + 1, ops=ops,
                   n=args.numel or N, pc_div=args.pc_div)
-    for opt in ("reduce_engine", "twoshot_mode"):
+    for opt in ("reduce_engine", "twoshot_mode", "gather_engine"):
         step_b.pad.set_option(opt, step.pad.get_option(opt))
     e2e_steps_p = 2 * e2e_steps
     with torch.cuda.stream(stream):
@@ -857,7 +861,7 @@ def run_gpu(args, rank, world, local_rank):
         "data": "synthetic (seeded torch RNG on the device; N(0,1) ranks, N(0,0.02) layer shards)",
         "config": {"workload": workload_name(ops, step.n, args.pc_div),
                    "reduce_engine": args.reduce_engine, "twoshot_mode": args.twoshot_mode,
-                   "W": W, "numel_per_rank": step.n, "bytes_per_step": step_bytes,
+                   "gather_engine": args.gather_engine, "W": W, "numel_per_rank": step.n, "bytes_per_step": step_bytes,
                    "l2": "inputs larger than L2 (every op >= 288 MiB of its own buffers; L2 129 MB)",
                    "parallelism": f"replicas x{world} (no inter-GPU collective; W ranks emulated per GPU)"},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(dom_gbs, 1), "peak": peak,
@@ -1039,6 +1043,8 @@ def main():
                     help="allreduce engine (pad option reduce_engine)")
     ap.add_argument("--twoshot-mode", choices=("auto", "pull", "push"), default="auto",
                     help="two-shot allgather phase (pad option twoshot_mode)")
+    ap.add_argument("--gather-engine", choices=GATHER_ENGINES, default="auto",
+                    help="gather engine (pad option gather_engine)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
