@@ -574,6 +574,8 @@ class FsdpLayers:
         self.calls = [rr.bound_call("rr_allgather_param_contiguous", [self.X[l, r].data_ptr() for r in range(W)],
                                     [self.Y[l].data_ptr()] + [None] * (W - 1), W, self._sp, len(self.splits),
                                     rr.RR_BF16, self.pad, stream.cuda_stream) for l in range(self.L)]
+        # the shards are drawn on the default stream; the gathers run on `stream`
+        torch.cuda.synchronize()
 
     def one_pass(self, per_layer=False):
         L, stream = self.L, self.stream
