@@ -356,7 +356,7 @@ KernelChoice gather_kernel_for(int engine, bool list)
                             kTmaThreads, kTmaSmem, 2};
     // As many blocks as fit (four per SM at 62 registers).  Three per SM
     // gathered one FSDP layer 2-3% faster, but layers now run on the bulk-copy
-    // kernel, and below 16 MiB per rank the two plans are within 0.7 us.
+    // kernel, and where this kernel runs now the two plans are within 0.7 us.
     return KernelChoice{list ? (const void *)gather_kernel_ldst<GatherListArgs>
                              : (const void *)gather_kernel_ldst<GatherArgs>,
                         kLdstThreads, 0};

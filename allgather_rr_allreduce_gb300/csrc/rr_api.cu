@@ -452,16 +452,21 @@ rr_status gather_prepare(const void *const *rank_bufs, int W, const int64_t *spl
     return RR_OK;
 }
 
-// Automatic gather engine.  Bulk copies from 16 MiB per rank up, when every
-// split boundary sits on a multiple of 16 bytes (the bases are checked
-// aligned, so the bulk engine then takes every byte); loads/stores otherwise.
-// Measured at W=8, rank-major, us per call (loads/stores, bulk copies): 8 MiB
-// 28.8 / 29.9, 16 MiB 49.5 / 48.5, 32 MiB 90.1 / 86.5, 512 MiB 1318 / 1251;
-// 28 FSDP layers back to back 153-154 / 146 us per layer.
-constexpr int64_t kBulkGatherMinShard = (int64_t)16 << 20;
+// Automatic gather engine.  Bulk copies when a call moves at least 256 MiB
+// (shards read plus outputs written) and every split boundary sits on a
+// multiple of 16 bytes (the bases are checked aligned, so the bulk engine
+// then takes every byte); loads/stores otherwise.  Measured, rank-major,
+// rank 0's output, us per call (loads/stores, bulk copies): at W=8, 8 MiB per
+// rank 28.8 / 29.9, 16 MiB 49.5 / 48.5, 32 MiB 90.1 / 86.5, 512 MiB 1318 /
+// 1251; 28 FSDP layers 153-154 / 146 per layer.  Around 128 MiB moved the
+// bulk engine loses at every W (W=2 32 MiB per rank 24.7 / 29.6, W=4 16 MiB
+// 25.2 / 29.4, W=16 4 MiB 22.7 / 29.0); from 256 MiB up it ties or wins
+// (W=4 32 MiB 51.1 / 49.0, W=16 8 MiB 49.4 / 49.2, 16 MiB 90.0 / 86.8).
+constexpr int64_t kBulkGatherMinBytes = (int64_t)256 << 20;
 int auto_gather_engine(const rr::GatherArgs &a, int64_t shard)
 {
-    if (shard < kBulkGatherMinShard) return 1;
+    const int64_t moved = shard * a.W * (1 + a.nout);
+    if (moved < kBulkGatherMinBytes) return 1;
     for (int s = 0; s <= a.nsplit; ++s)
         if (a.off[s] & 15) return 1;
     return 2;

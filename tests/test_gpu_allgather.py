@@ -121,29 +121,33 @@ def test_param_contiguous_fixed_blocks(rr, engine, blocks):
 
 
 AUTO_CASES = {
-    # (splits per rank in bf16 elements (None = rank-major), numel, engine expected)
-    "rank_major_16MiB": (None, 8 << 20, 2),
-    "rank_major_16MiB_less_16B": (None, (8 << 20) - 8, 1),
-    "param_aligned": ([3 << 20, 8, 5 << 20, 4096], None, 2),
-    "param_split_off_16B": ([3 << 20, 9, 5 << 20, 4096], None, 1),
-    "rank_major_1MiB": (None, 1 << 19, 1),
+    # (W, splits per rank in bf16 elements (None = rank-major), numel, kept outputs, engine expected);
+    # bulk copies from 256 MiB moved per call (shards read + outputs written)
+    "W8_16MiB": (8, None, 8 << 20, (0,), 2),
+    "W8_16MiB_less_16B": (8, None, (8 << 20) - 8, (0,), 1),
+    "W8_param_aligned": (8, [3 << 20, 8, 5 << 20, 4096], None, (0,), 2),
+    "W8_param_split_off_16B": (8, [3 << 20, 9, 5 << 20, 4096], None, (0,), 1),
+    "W8_1MiB": (8, None, 1 << 19, (0,), 1),
+    "W8_11MiB_two_outputs": (8, None, 11 << 19, (0, 6), 2),
+    "W2_32MiB": (2, None, 16 << 20, (1,), 1),
+    "W2_64MiB": (2, None, 32 << 20, (1,), 2),
 }
 
 
 @pytest.mark.parametrize("case", list(AUTO_CASES))
 def test_automatic_engine_choice(rr, case):
-    """The automatic gather engine: bulk copies from 16 MiB per rank up when
-    every split boundary is a multiple of 16 bytes, loads/stores otherwise;
-    the bytes equal the oracle's either way."""
-    splits, numel, expect = AUTO_CASES[case]
-    W, dtype = 8, "bf16"
+    """The automatic gather engine: bulk copies when a call moves at least
+    256 MiB and every split boundary is a multiple of 16 bytes, loads/stores
+    otherwise; the bytes equal the oracle's either way."""
+    W, splits, numel, keep, expect = AUTO_CASES[case]
+    dtype = "bf16"
     pad = pad_for(rr, W)
     pad.set_option("gather_engine", 0)
     n = numel if splits is None else sum(splits)
     ins = workloads.rank_buffers(W, n, dtype, "bits", seed_base=77)
     bufs = RankBuffers(W, n, dtype)
     bufs.fill(ins)
-    outs = GuardedOutputs(W, W * n, dtype, materialise=(0, 6))
+    outs = GuardedOutputs(W, W * n, dtype, materialise=keep)
     if splits is None:
         want = oracle.allgather_rank_major(ins, dtype)
         rr.rr_allgather(bufs.ptrs, outs.ptrs, W, n, dtype, pad)
@@ -152,7 +156,7 @@ def test_automatic_engine_choice(rr, case):
         rr.rr_allgather_param_contiguous(bufs.ptrs, outs.ptrs, W, splits, dtype, pad)
     pad.status()
     assert pad.get_option("last_engine") == expect
-    for q in (0, 6):
+    for q in keep:
         assert_bitwise(outs.host(q), want, f"{case} output {q}")
     outs.check_guards()
 
