@@ -283,6 +283,21 @@ rr_status check_iterating(const rr_signal_pad *pad)
     return RR_OK;
 }
 
+// Automatic engine of copy_mode: the bulk-copy staging kernel or the
+// load/store kernels, by W and bytes per rank.  Measured, bf16, us per call
+// (staged / loads-stores): one-shot, rank 0's output, W=2 1..64 MiB per rank
+// always slower staged (64 MiB 92.5 / 71.2); W=4 8 MiB 22.8 / 18.6, 16 MiB
+// 35.0 / 35.4, 64 MiB 113.1 / 127.1; W=8 2 MiB 14.9 / 13.5, 8 MiB 31.1 /
+// 35.9, 32 MiB 103 / 135; W=16 2 MiB 20.6 / 19.8, 4 MiB 31.0 / 38.9.
+// Two-shot, all outputs: W=2 always faster staged (1 MiB 11.6 / 12.5, 64 MiB
+// 83.4 / 141.6); W=4 4 MiB 18.4 / 16.9, 8 MiB 25.1 / 29.1; W=8 2 MiB 18.6 /
+// 15.7, 8 MiB 42.3 / 46.9; W=16 2 MiB 28.7 / 24.6, 8 MiB 80.6 / 83.7.
+bool auto_staged(bool twoshot, int W, int64_t bytes_per_rank)
+{
+    if (twoshot) return W <= 2 || bytes_per_rank >= ((int64_t)8 << 20);
+    return W >= 4 && (int64_t)W * bytes_per_rank >= ((int64_t)64 << 20);
+}
+
 rr_status allreduce_common(bool twoshot, const void *const *inputs, void *const *rank_bufs,
                            void *const *outputs, int W, int64_t numel, rr_dtype dtype, int copy_mode,
                            rr_signal_pad *pad, cudaStream_t stream)
@@ -356,11 +371,12 @@ rr_status allreduce_common(bool twoshot, const void *const *inputs, void *const 
 
     const bool push = pad->twoshot_mode != 1;
     // bulk-copy engine: one-shot loads (copy_mode off), or staging by a
-    // producer warp (copy_mode on; for the two-shot only with the push allgather)
-    // automatic: bulk-copy staging for copy_mode (measured faster than the
-    // load/store kernels: 105 vs 135 us one-shot, 144 vs 176 us two-shot at
-    // W=8 x 32 MiB bf16), loads/stores otherwise
-    const bool tma = copy_mode ? (pad->reduce_engine != 1 && (!twoshot || push))
+    // producer warp (copy_mode on; for the two-shot only with the push
+    // allgather).  Automatic: see auto_staged for copy_mode, loads/stores
+    // otherwise.  In-launch iterations always stage by bulk copies.
+    const bool tma = copy_mode ? ((!twoshot || push) &&
+                                  (iterate || pad->reduce_engine == 2 ||
+                                   (pad->reduce_engine == 0 && auto_staged(twoshot, W, bytes))))
                                : (!twoshot && pad->reduce_engine == 2);
     const rr::KernelChoice k = iterate ? rr::iter_reduce_kernel_for(twoshot, W, copy_mode != 0)
                                : tma ? (copy_mode ? rr::staged_kernel_for(dtype, W, twoshot)

@@ -452,3 +452,35 @@ def test_argument_errors(rr):
     assert e.value.status == rr.RR_ERR_INVALID_ARG
     pad.status()
     outs.check_guards()
+
+
+AUTO_COPY_CASES = {
+    # (algo, W, bf16 elements per rank, engine expected); 2 = staged bulk-copy kernel, 1 = loads/stores
+    "oneshot_W2_16MiB": ("oneshot", 2, 8 << 20, 1),
+    "oneshot_W4_8MiB": ("oneshot", 4, 4 << 20, 1),
+    "oneshot_W4_16MiB": ("oneshot", 4, 8 << 20, 2),
+    "oneshot_W8_8MiB": ("oneshot", 8, 4 << 20, 2),
+    "oneshot_W16_2MiB": ("oneshot", 16, 1 << 20, 1),
+    "twoshot_W2_1MiB": ("twoshot", 2, 1 << 19, 2),
+    "twoshot_W8_4MiB": ("twoshot", 8, 2 << 20, 1),
+    "twoshot_W8_8MiB": ("twoshot", 8, 4 << 20, 2),
+    "twoshot_pull_W8_8MiB": ("twoshot_pull", 8, 4 << 20, 1),
+}
+
+
+@pytest.mark.parametrize("case", list(AUTO_COPY_CASES))
+def test_automatic_copy_mode_engine(rr, case):
+    """copy_mode on the automatic engine: the staged kernel for the one-shot
+    when W >= 4 and W x bytes per rank >= 64 MiB, for the push two-shot when
+    W = 2 or from 8 MiB per rank; the load/store kernels otherwise.  The sums
+    equal the oracle's either way."""
+    algo, W, N, expect = AUTO_COPY_CASES[case]
+    ins = workloads.rank_buffers(W, N, "bf16", "normal", seed_base=4100 + W)
+    want = oracle.allreduce(ins, "bf16")
+    pad = pad_for(rr, W)
+    pad.set_option("reduce_engine", 0)
+    _, _, outs = run_allreduce(rr, algo, W, N, "bf16", 1, ins, materialise=(0,) if algo == "oneshot" else None)
+    assert pad.get_option("last_engine") == expect
+    for r in ((0,) if algo == "oneshot" else range(W)):
+        assert_bitwise(outs.host(r), want, f"{case} output {r}")
+    outs.check_guards()
