@@ -298,6 +298,18 @@ bool auto_staged(bool twoshot, int W, int64_t bytes_per_rank)
     return W >= 4 && (int64_t)W * bytes_per_rank >= ((int64_t)64 << 20);
 }
 
+// Automatic engine of the one-shot with copy_mode off: bulk-copy loads into a
+// shared-memory ring when W > 8 and each output reads at least 128 MiB,
+// loads/stores otherwise.  Measured, bf16, rank 0's output, us per call
+// (loads-stores / bulk): W <= 8 always faster with loads/stores (W=8 32 MiB
+// per rank 50.4 / 53.9, 64 MiB 92.3 / 98.5); W=10 8 MiB 16.5 / 22.7, 32 MiB
+// 69.9 / 67.6; W=12 8 MiB 23.0 / 26.3, 32 MiB 77.0 / 74.8; W=14 8 MiB 30.8 /
+// 28.7; W=16 4 MiB 12.4 / 18.5, 8 MiB 32.9 / 30.1, 64 MiB 183.4 / 168.6.
+bool auto_bulk_oneshot(int W, int64_t bytes_per_rank)
+{
+    return W > 8 && (int64_t)W * bytes_per_rank >= ((int64_t)128 << 20);
+}
+
 rr_status allreduce_common(bool twoshot, const void *const *inputs, void *const *rank_bufs,
                            void *const *outputs, int W, int64_t numel, rr_dtype dtype, int copy_mode,
                            rr_signal_pad *pad, cudaStream_t stream)
@@ -372,12 +384,14 @@ rr_status allreduce_common(bool twoshot, const void *const *inputs, void *const 
     const bool push = pad->twoshot_mode != 1;
     // bulk-copy engine: one-shot loads (copy_mode off), or staging by a
     // producer warp (copy_mode on; for the two-shot only with the push
-    // allgather).  Automatic: see auto_staged for copy_mode, loads/stores
-    // otherwise.  In-launch iterations always stage by bulk copies.
+    // allgather).  Automatic: auto_staged with copy_mode, auto_bulk_oneshot
+    // without.  In-launch iterations always stage by bulk copies (copy_mode)
+    // and reduce with loads/stores (copy_mode off).
     const bool tma = copy_mode ? ((!twoshot || push) &&
                                   (iterate || pad->reduce_engine == 2 ||
                                    (pad->reduce_engine == 0 && auto_staged(twoshot, W, bytes))))
-                               : (!twoshot && pad->reduce_engine == 2);
+                               : (!twoshot && (pad->reduce_engine == 2 ||
+                                               (pad->reduce_engine == 0 && !iterate && auto_bulk_oneshot(W, bytes))));
     const rr::KernelChoice k = iterate ? rr::iter_reduce_kernel_for(twoshot, W, copy_mode != 0)
                                : tma ? (copy_mode ? rr::staged_kernel_for(dtype, W, twoshot)
                                                   : rr::oneshot_tma_kernel_for(dtype, W))

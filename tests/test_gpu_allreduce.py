@@ -484,3 +484,29 @@ def test_automatic_copy_mode_engine(rr, case):
     for r in ((0,) if algo == "oneshot" else range(W)):
         assert_bitwise(outs.host(r), want, f"{case} output {r}")
     outs.check_guards()
+
+
+AUTO_OFF_CASES = {
+    # (W, bf16 elements per rank, engine expected) for the one-shot with copy_mode off
+    "W16_8MiB": (16, 4 << 20, 2),
+    "W16_4MiB": (16, 2 << 20, 1),
+    "W10_16MiB": (10, 8 << 20, 2),
+    "W8_32MiB": (8, 16 << 20, 1),
+}
+
+
+@pytest.mark.parametrize("case", list(AUTO_OFF_CASES))
+def test_automatic_oneshot_engine_copy_off(rr, case):
+    """The one-shot with copy_mode off on the automatic engine: bulk-copy
+    loads when W > 8 and W x bytes per rank >= 128 MiB, loads/stores
+    otherwise; the sums equal the oracle's either way."""
+    W, N, expect = AUTO_OFF_CASES[case]
+    ins = workloads.rank_buffers(W, N, "bf16", "normal", seed_base=4300 + W)
+    want = oracle.allreduce(ins, "bf16")
+    pad = pad_for(rr, W)
+    pad.set_option("reduce_engine", 0)
+    _, _, outs = run_allreduce(rr, "oneshot", W, N, "bf16", 0, ins, materialise=(0, W - 1))
+    assert pad.get_option("last_engine") == expect
+    for r in (0, W - 1):
+        assert_bitwise(outs.host(r), want, f"{case} output {r}")
+    outs.check_guards()
