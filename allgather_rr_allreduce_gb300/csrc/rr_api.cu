@@ -283,33 +283,6 @@ rr_status check_iterating(const rr_signal_pad *pad)
     return RR_OK;
 }
 
-// Automatic engine of copy_mode: the bulk-copy staging kernel or the
-// load/store kernels, by W and bytes per rank.  Measured, bf16, us per call
-// (staged / loads-stores): one-shot, rank 0's output, W=2 1..64 MiB per rank
-// always slower staged (64 MiB 92.5 / 71.2); W=4 8 MiB 22.8 / 18.6, 16 MiB
-// 35.0 / 35.4, 64 MiB 113.1 / 127.1; W=8 2 MiB 14.9 / 13.5, 8 MiB 31.1 /
-// 35.9, 32 MiB 103 / 135; W=16 2 MiB 20.6 / 19.8, 4 MiB 31.0 / 38.9.
-// Two-shot, all outputs: W=2 always faster staged (1 MiB 11.6 / 12.5, 64 MiB
-// 83.4 / 141.6); W=4 4 MiB 18.4 / 16.9, 8 MiB 25.1 / 29.1; W=8 2 MiB 18.6 /
-// 15.7, 8 MiB 42.3 / 46.9; W=16 2 MiB 28.7 / 24.6, 8 MiB 80.6 / 83.7.
-bool auto_staged(bool twoshot, int W, int64_t bytes_per_rank)
-{
-    if (twoshot) return W <= 2 || bytes_per_rank >= ((int64_t)8 << 20);
-    return W >= 4 && (int64_t)W * bytes_per_rank >= ((int64_t)64 << 20);
-}
-
-// Automatic engine of the one-shot with copy_mode off: bulk-copy loads into a
-// shared-memory ring when W > 8 and each output reads at least 128 MiB,
-// loads/stores otherwise.  Measured, bf16, rank 0's output, us per call
-// (loads-stores / bulk): W <= 8 always faster with loads/stores (W=8 32 MiB
-// per rank 50.4 / 53.9, 64 MiB 92.3 / 98.5); W=10 8 MiB 16.5 / 22.7, 32 MiB
-// 69.9 / 67.6; W=12 8 MiB 23.0 / 26.3, 32 MiB 77.0 / 74.8; W=14 8 MiB 30.8 /
-// 28.7; W=16 4 MiB 12.4 / 18.5, 8 MiB 32.9 / 30.1, 64 MiB 183.4 / 168.6.
-bool auto_bulk_oneshot(int W, int64_t bytes_per_rank)
-{
-    return W > 8 && (int64_t)W * bytes_per_rank >= ((int64_t)128 << 20);
-}
-
 rr_status allreduce_common(bool twoshot, const void *const *inputs, void *const *rank_bufs,
                            void *const *outputs, int W, int64_t numel, rr_dtype dtype, int copy_mode,
                            rr_signal_pad *pad, cudaStream_t stream)
@@ -389,9 +362,9 @@ rr_status allreduce_common(bool twoshot, const void *const *inputs, void *const 
     // and reduce with loads/stores (copy_mode off).
     const bool tma = copy_mode ? ((!twoshot || push) &&
                                   (iterate || pad->reduce_engine == 2 ||
-                                   (pad->reduce_engine == 0 && auto_staged(twoshot, W, bytes))))
+                                   (pad->reduce_engine == 0 && rr::auto_staged(twoshot, W, bytes))))
                                : (!twoshot && (pad->reduce_engine == 2 ||
-                                               (pad->reduce_engine == 0 && !iterate && auto_bulk_oneshot(W, bytes))));
+                                               (pad->reduce_engine == 0 && !iterate && rr::auto_bulk_oneshot(W, bytes))));
     const rr::KernelChoice k = iterate ? rr::iter_reduce_kernel_for(twoshot, W, copy_mode != 0)
                                : tma ? (copy_mode ? rr::staged_kernel_for(dtype, W, twoshot)
                                                   : rr::oneshot_tma_kernel_for(dtype, W))
@@ -482,26 +455,6 @@ rr_status gather_prepare(const void *const *rank_bufs, int W, const int64_t *spl
     return RR_OK;
 }
 
-// Automatic gather engine.  Bulk copies when a call moves at least 256 MiB
-// (shards read plus outputs written) and every split boundary sits on a
-// multiple of 16 bytes (the bases are checked aligned, so the bulk engine
-// then takes every byte); loads/stores otherwise.  Measured, rank-major,
-// rank 0's output, us per call (loads/stores, bulk copies): at W=8, 8 MiB per
-// rank 28.8 / 29.9, 16 MiB 49.5 / 48.5, 32 MiB 90.1 / 86.5, 512 MiB 1318 /
-// 1251; 28 FSDP layers 153-154 / 146 per layer.  Around 128 MiB moved the
-// bulk engine loses at every W (W=2 32 MiB per rank 24.7 / 29.6, W=4 16 MiB
-// 25.2 / 29.4, W=16 4 MiB 22.7 / 29.0); from 256 MiB up it ties or wins
-// (W=4 32 MiB 51.1 / 49.0, W=16 8 MiB 49.4 / 49.2, 16 MiB 90.0 / 86.8).
-constexpr int64_t kBulkGatherMinBytes = (int64_t)256 << 20;
-int auto_gather_engine(const rr::GatherArgs &a, int64_t shard)
-{
-    const int64_t moved = shard * a.W * (1 + a.nout);
-    if (moved < kBulkGatherMinBytes) return 1;
-    for (int s = 0; s <= a.nsplit; ++s)
-        if (a.off[s] & 15) return 1;
-    return 2;
-}
-
 // Enqueue a gather whose arguments are complete but for B and the signal
 // arguments.  Engine 3 (copy engines) issues one cudaMemcpyAsync per
 // (materialised output, rank, param) slot instead of a kernel: stream order
@@ -512,7 +465,7 @@ rr_status run_gather(rr_signal_pad *pad, Args &a, int64_t shard, bool list, cuda
 {
     rr_status st = check_device(pad);
     if (st != RR_OK) return st;
-    const int engine = pad->engine != 0 ? pad->engine : auto_gather_engine(a, shard);
+    const int engine = pad->engine != 0 ? pad->engine : rr::auto_gather_engine(a, shard);
     const bool iterate = iterating(pad);
     if (iterate) {
         st = check_iterating(pad);

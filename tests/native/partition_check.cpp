@@ -168,6 +168,43 @@ int main()
         }
     }
 
+    // Automatic engines: the rules at their boundaries.
+    const int64_t MiB = (int64_t)1 << 20;
+    CHECK(!auto_staged(false, 2, 64 * MiB) && !auto_staged(false, 2, 1024 * MiB), "one-shot W=2 staged\n");
+    CHECK(!auto_staged(false, 4, 16 * MiB - 16) && auto_staged(false, 4, 16 * MiB), "one-shot W=4 boundary\n");
+    CHECK(!auto_staged(false, 8, 8 * MiB - 16) && auto_staged(false, 8, 8 * MiB), "one-shot W=8 boundary\n");
+    CHECK(!auto_staged(false, 16, 4 * MiB - 16) && auto_staged(false, 16, 4 * MiB), "one-shot W=16 boundary\n");
+    CHECK(auto_staged(true, 2, 16) && auto_staged(true, 1, 16), "two-shot W<=2 not staged\n");
+    CHECK(!auto_staged(true, 4, 8 * MiB - 16) && auto_staged(true, 4, 8 * MiB) && auto_staged(true, 16, 8 * MiB),
+          "two-shot 8 MiB boundary\n");
+    CHECK(!auto_bulk_oneshot(8, 1024 * MiB) && !auto_bulk_oneshot(2, 1024 * MiB), "copy-off bulk one-shot at W<=8\n");
+    CHECK(!auto_bulk_oneshot(16, 8 * MiB - 16) && auto_bulk_oneshot(16, 8 * MiB) && auto_bulk_oneshot(9, 15 * MiB),
+          "copy-off bulk one-shot boundary\n");
+    {
+        GatherArgs g{};
+        g.W = 8;
+        g.nout = 1;
+        g.nsplit = 1;
+        g.off[0] = 0;
+        g.off[1] = 16 * MiB;
+        CHECK(auto_gather_engine(g, 16 * MiB) == 2, "gather 256 MiB moved not bulk\n");
+        g.off[1] = 16 * MiB - 16;
+        CHECK(auto_gather_engine(g, 16 * MiB - 16) == 1, "gather below 256 MiB moved is bulk\n");
+        g.nout = 2;  // 24 x 11 MiB = 264 MiB moved
+        g.off[1] = 11 * MiB;
+        CHECK(auto_gather_engine(g, 11 * MiB) == 2, "gather with two outputs not bulk\n");
+        g.nsplit = 2;
+        g.off[1] = 5 * MiB + 8;  // a split boundary off 16 bytes
+        g.off[2] = 11 * MiB;
+        CHECK(auto_gather_engine(g, 11 * MiB) == 1, "gather with a split off 16 bytes is bulk\n");
+        g.W = 2;
+        g.nout = 1;
+        g.nsplit = 1;
+        g.off[1] = 32 * MiB;
+        CHECK(auto_gather_engine(g, 32 * MiB) == 1 && (g.off[1] = 64 * MiB, auto_gather_engine(g, 64 * MiB) == 2),
+              "gather W=2 boundary\n");
+    }
+
     if (failures) {
         std::printf("%d failures\n", failures);
         return 1;
