@@ -465,6 +465,9 @@ AUTO_COPY_CASES = {
     "twoshot_W8_4MiB": ("twoshot", 8, 2 << 20, 1),
     "twoshot_W8_8MiB": ("twoshot", 8, 4 << 20, 2),
     "twoshot_pull_W8_8MiB": ("twoshot_pull", 8, 4 << 20, 1),
+    "oneshot_W16_4MiB": ("oneshot", 16, 2 << 20, 2),
+    "twoshot_W16_8MiB_ragged": ("twoshot", 16, (4 << 20) + 13, 2),
+    "twoshot_W2_ragged": ("twoshot", 2, 300_007, 2),
 }
 
 
@@ -492,6 +495,7 @@ AUTO_OFF_CASES = {
     "W16_4MiB": (16, 2 << 20, 1),
     "W10_16MiB": (10, 8 << 20, 2),
     "W8_32MiB": (8, 16 << 20, 1),
+    "W12_11MiB_ragged": (12, (11 << 19) + 5, 2),
 }
 
 
