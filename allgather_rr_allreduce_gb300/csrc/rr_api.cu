@@ -241,11 +241,17 @@ rr_status launch(rr_signal_pad *pad, const rr::KernelChoice &k, int grid, const 
     cfg.blockDim = dim3((unsigned)k.threads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)k.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    // Cooperative (every block resident at once) and programmatic (the grid
+    // may be launched while the previous one in the stream drains; every
+    // kernel waits for it in begin_call before touching memory): graph-replayed
+    // calls at W=8 take 0.2-0.65 us less from 16 to 256 KiB per rank.
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     void *params[1] = {const_cast<Args *>(&args)};
     cudaError_t e = cudaLaunchKernelExC(&cfg, k.fn, params);
     if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC");
@@ -1019,11 +1025,17 @@ extern "C" rr_status rr_allreduce_oneshot_noalloc(const void *const *inputs, voi
     cfg.blockDim = dim3((unsigned)k.threads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)k.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    // Cooperative (every block resident at once) and programmatic (the grid
+    // may be launched while the previous one in the stream drains; every
+    // kernel waits for it in begin_call before touching memory): graph-replayed
+    // calls at W=8 take 0.2-0.65 us less from 16 to 256 KiB per rank.
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     void *params[1] = {&a};
     e = cudaLaunchKernelExC(&cfg, k.fn, params);
     if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC");

@@ -334,6 +334,12 @@ __device__ __forceinline__ uint64_t next_generation(uint64_t g64)
 
 __device__ __forceinline__ SignalArgs begin_call(const SignalArgs &in)
 {
+    // Launches are programmatic (the next kernel in the stream may start
+    // before this one ends): wait until the previous grid has completed and
+    // its writes are visible before touching memory, then let the next one
+    // launch.  Without a programmatic launch both are no-ops.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     SignalArgs s = in;
     if (s.dev_gen) {
         const uint64_t g64 = next_generation(*(volatile uint64_t *)s.dev_gen);
