@@ -31,7 +31,12 @@
  *    pads, because a pad's flag slots and generation counter are shared
  *    state (the lesson of the shared per-slot flag in "ccl: hierarchical
  *    cross-node AllGather (intra-node SDMA + inter-node RDMA) #441", the
- *    commit on concurrent param-contiguous scatters).
+ *    commit on concurrent param-contiguous scatters).  Each call is one
+ *    cooperative kernel launch that is also programmatic: it may be launched
+ *    while the work before it on `stream` drains, and waits on the device
+ *    for that work to complete before touching memory, so stream order is
+ *    kept; the kernel lets the next launch on `stream` start early, which a
+ *    following launch uses only if it is programmatic too.
  *  - Reductions accumulate in binary32 in rank order 0, 1, ..., W-1, starting
  *    from rank 0's value, and round once to the element type (round to
  *    nearest, ties to even; no flush of subnormals).  int32 sums wrap modulo
