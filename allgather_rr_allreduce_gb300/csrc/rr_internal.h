@@ -336,7 +336,8 @@ inline bool auto_bulk_oneshot(int W, int64_t bytes_per_rank)
 }
 
 // Automatic gather engine.  Bulk copies when a call moves at least 256 MiB
-// (shards read plus outputs written) and every split boundary sits on a
+// (shards read plus outputs written; 8 MiB with two or more kept outputs)
+// and every split boundary sits on a
 // multiple of 16 bytes (the bases are checked aligned, so the bulk engine
 // then takes every byte); loads/stores otherwise.  Measured, rank-major,
 // rank 0's output, us per call (loads/stores, bulk copies): at W=8, 8 MiB per
@@ -345,11 +346,17 @@ inline bool auto_bulk_oneshot(int W, int64_t bytes_per_rank)
 // bulk engine loses at every W (W=2 32 MiB per rank 24.7 / 29.6, W=4 16 MiB
 // 25.2 / 29.4, W=16 4 MiB 22.7 / 29.0); from 256 MiB up it ties or wins
 // (W=4 32 MiB 51.1 / 49.0, W=16 8 MiB 49.4 / 49.2, 16 MiB 90.0 / 86.8).
+// With two or more kept outputs the bulk engine also wins below that, from
+// 8 MiB moved (W=8, 8 outputs: 256 KiB per rank 16.2 / 11.9, 1 MiB 18.6 /
+// 17.1, 32 MiB 409.1 / 399.7; W=4, 4 outputs: 1 MiB 14.2 / 10.6; W=8, 2
+// outputs: 1 MiB 12.2 / 11.1, 16 MiB 72.0 / 73.6; below 8 MiB moved the two
+// tie or loads/stores lead).
 constexpr int64_t kBulkGatherMinBytes = (int64_t)256 << 20;
+constexpr int64_t kBulkGatherMinBytesMulti = (int64_t)8 << 20;
 inline int auto_gather_engine(const GatherArgs &a, int64_t shard)
 {
     const int64_t moved = shard * a.W * (1 + a.nout);
-    if (moved < kBulkGatherMinBytes) return 1;
+    if (moved < (a.nout >= 2 ? kBulkGatherMinBytesMulti : kBulkGatherMinBytes)) return 1;
     for (int s = 0; s <= a.nsplit; ++s)
         if (a.off[s] & 15) return 1;
     return 2;

@@ -84,7 +84,8 @@ typedef enum {
     RR_OPT_TIMEOUT_NS = 0,      /* barrier wait limit in ns (default 2e9) */
     RR_OPT_BLOCKS_PER_RANK = 1, /* 0 = automatic (default); else a fixed block count per rank */
     RR_OPT_GATHER_ENGINE = 2,   /* 0 = automatic (TMA bulk copies when a call moves at least
-                                   256 MiB, shards read plus outputs written, and every split
+                                   256 MiB, shards read plus outputs written, or 8 MiB with two
+                                   or more kept outputs, and every split
                                    boundary is a multiple of 16 bytes; 128-bit loads/stores
                                    otherwise), 1 = 128-bit loads/stores,
                                    2 = TMA bulk copies, 3 = the GPU's copy engines: one

@@ -193,6 +193,10 @@ int main()
         g.nout = 2;  // 24 x 11 MiB = 264 MiB moved
         g.off[1] = 11 * MiB;
         CHECK(auto_gather_engine(g, 11 * MiB) == 2, "gather with two outputs not bulk\n");
+        g.off[1] = (MiB / 3) & ~(int64_t)15;  // 24 x 349,520 B: just under 8 MiB moved
+        CHECK(auto_gather_engine(g, g.off[1]) == 1, "gather with two outputs below 8 MiB moved is bulk\n");
+        g.off[1] = MiB;  // 24 MiB moved
+        CHECK(auto_gather_engine(g, MiB) == 2, "gather with two outputs from 8 MiB moved not bulk\n");
         g.nsplit = 2;
         g.off[1] = 5 * MiB + 8;  // a split boundary off 16 bytes
         g.off[2] = 11 * MiB;

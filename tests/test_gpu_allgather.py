@@ -131,14 +131,18 @@ AUTO_CASES = {
     "W8_11MiB_two_outputs": (8, None, 11 << 19, (0, 6), 2),
     "W2_32MiB": (2, None, 16 << 20, (1,), 1),
     "W2_64MiB": (2, None, 32 << 20, (1,), 2),
+    "W8_1MiB_all_outputs": (8, None, 1 << 19, tuple(range(8)), 2),
+    "W8_128KiB_two_outputs": (8, None, 1 << 16, (0, 5), 1),
+    "W4_param_2MiB_two_outputs": (4, [1 << 19, 24, (1 << 19) - 24], None, (1, 2), 2),
 }
 
 
 @pytest.mark.parametrize("case", list(AUTO_CASES))
 def test_automatic_engine_choice(rr, case):
     """The automatic gather engine: bulk copies when a call moves at least
-    256 MiB and every split boundary is a multiple of 16 bytes, loads/stores
-    otherwise; the bytes equal the oracle's either way."""
+    256 MiB (8 MiB with two or more kept outputs) and every split boundary is
+    a multiple of 16 bytes, loads/stores otherwise; the bytes equal the
+    oracle's either way."""
     W, splits, numel, keep, expect = AUTO_CASES[case]
     dtype = "bf16"
     pad = pad_for(rr, W)
