@@ -368,9 +368,9 @@ rr_status allreduce_common(bool twoshot, const void *const *inputs, void *const 
     // and reduce with loads/stores (copy_mode off).
     const bool tma = copy_mode ? ((!twoshot || push) &&
                                   (iterate || pad->reduce_engine == 2 ||
-                                   (pad->reduce_engine == 0 && rr::auto_staged(twoshot, W, bytes))))
+                                   (pad->reduce_engine == 0 && rr::auto_staged(twoshot, W, bytes, nout))))
                                : (!twoshot && (pad->reduce_engine == 2 ||
-                                               (pad->reduce_engine == 0 && !iterate && rr::auto_bulk_oneshot(W, bytes))));
+                                               (pad->reduce_engine == 0 && !iterate && rr::auto_bulk_oneshot(W, bytes, nout))));
     const rr::KernelChoice k = iterate ? rr::iter_reduce_kernel_for(twoshot, W, copy_mode != 0)
                                : tma ? (copy_mode ? rr::staged_kernel_for(dtype, W, twoshot)
                                                   : rr::oneshot_tma_kernel_for(dtype, W))

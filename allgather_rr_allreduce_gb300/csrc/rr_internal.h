@@ -314,25 +314,35 @@ KernelChoice iter_gather_kernel_for(int engine, bool list);
 // always slower staged (64 MiB 92.5 / 71.2); W=4 8 MiB 22.8 / 18.6, 16 MiB
 // 35.0 / 35.4, 64 MiB 113.1 / 127.1; W=8 2 MiB 14.9 / 13.5, 8 MiB 31.1 /
 // 35.9, 32 MiB 103 / 135; W=16 2 MiB 20.6 / 19.8, 4 MiB 31.0 / 38.9.
+// The staged one-shot loses once many outputs are kept, each summed from all
+// W buffers by the consumer warps: 2 outputs, W=4 32 MiB 86.8 / 78.2, W=8 32
+// MiB 123.5 / 162.3, W=16 8 MiB 73.0 / 85.4; all outputs, W=4 32 MiB 139.4 /
+// 107.9, W=8 32 MiB 355.7 / 363.5, W=16 8 MiB 337.9 / 295.8, 32 MiB 1588.8 /
+// 1214.7; so it runs with one kept output or at most W/4.
 // Two-shot, all outputs: W=2 always faster staged (1 MiB 11.6 / 12.5, 64 MiB
 // 83.4 / 141.6); W=4 4 MiB 18.4 / 16.9, 8 MiB 25.1 / 29.1; W=8 2 MiB 18.6 /
 // 15.7, 8 MiB 42.3 / 46.9; W=16 2 MiB 28.7 / 24.6, 8 MiB 80.6 / 83.7.
-inline bool auto_staged(bool twoshot, int W, int64_t bytes_per_rank)
+inline bool auto_staged(bool twoshot, int W, int64_t bytes_per_rank, int nout)
 {
     if (twoshot) return W <= 2 || bytes_per_rank >= ((int64_t)8 << 20);
-    return W >= 4 && (int64_t)W * bytes_per_rank >= ((int64_t)64 << 20);
+    return W >= 4 && (int64_t)W * bytes_per_rank >= ((int64_t)64 << 20) && (nout <= 1 || 4 * nout <= W);
 }
 
 // Automatic engine of the one-shot with copy_mode off: bulk-copy loads into a
-// shared-memory ring when W > 8 and each output reads at least 128 MiB,
-// loads/stores otherwise.  Measured, bf16, rank 0's output, us per call
+// shared-memory ring when W > 8 and each output reads at least 128 MiB (512
+// MiB with more than half the outputs kept), loads/stores otherwise.  Measured, bf16, rank 0's output, us per call
 // (loads-stores / bulk): W <= 8 always faster with loads/stores (W=8 32 MiB
 // per rank 50.4 / 53.9, 64 MiB 92.3 / 98.5); W=10 8 MiB 16.5 / 22.7, 32 MiB
 // 69.9 / 67.6; W=12 8 MiB 23.0 / 26.3, 32 MiB 77.0 / 74.8; W=14 8 MiB 30.8 /
 // 28.7; W=16 4 MiB 12.4 / 18.5, 8 MiB 32.9 / 30.1, 64 MiB 183.4 / 168.6.
-inline bool auto_bulk_oneshot(int W, int64_t bytes_per_rank)
+// Two kept outputs: the same (W=12 8 MiB 37.0 / 41.1, 32 MiB 143.5 / 139.3;
+// W=16 8 MiB 49.4 / 46.9).  All outputs: the bulk kernel wins later (W=12 32
+// MiB 799.0 / 798.6, W=16 8 MiB 265.1 / 310.9, 32 MiB 1361.7 / 1219.5), so
+// with more than half the outputs kept each output must read 512 MiB.
+inline bool auto_bulk_oneshot(int W, int64_t bytes_per_rank, int nout)
 {
-    return W > 8 && (int64_t)W * bytes_per_rank >= ((int64_t)128 << 20);
+    const int64_t need = (int64_t)(2 * nout > W ? 512 : 128) << 20;
+    return W > 8 && (int64_t)W * bytes_per_rank >= need;
 }
 
 // Automatic gather engine.  Bulk copies when a call moves at least 256 MiB

@@ -107,10 +107,11 @@ typedef enum {
                                    one-shot, 8 KiB per range two-shot).  Grown where a block
                                    would pass 65535 rounds */
     RR_OPT_REDUCE_ENGINE = 5,   /* 0 = automatic (copy_mode: bulk-copy staging for the one-shot
-                                   when W >= 4 and W x bytes per rank >= 64 MiB, for the push
-                                   two-shot when W = 2 or from 8 MiB per rank; copy_mode off:
-                                   bulk-copy loads for the one-shot when W > 8 and W x bytes
-                                   per rank >= 128 MiB; loads/stores otherwise),
+                                   when W >= 4, W x bytes per rank >= 64 MiB and one or at most
+                                   W/4 outputs are kept, for the push two-shot when W = 2 or
+                                   from 8 MiB per rank; copy_mode off: bulk-copy loads for the
+                                   one-shot when W > 8 and W x bytes per rank >= 128 MiB, 512 MiB
+                                   with more than half the outputs kept; loads/stores otherwise),
                                    1 = 128-bit loads/stores, 2 = bulk-copy (TMA)
                                    engine: copy_mode off, the one-shot's loads stream into a
                                    shared-memory ring; copy_mode on, a producer warp stages the

@@ -170,16 +170,22 @@ int main()
 
     // Automatic engines: the rules at their boundaries.
     const int64_t MiB = (int64_t)1 << 20;
-    CHECK(!auto_staged(false, 2, 64 * MiB) && !auto_staged(false, 2, 1024 * MiB), "one-shot W=2 staged\n");
-    CHECK(!auto_staged(false, 4, 16 * MiB - 16) && auto_staged(false, 4, 16 * MiB), "one-shot W=4 boundary\n");
-    CHECK(!auto_staged(false, 8, 8 * MiB - 16) && auto_staged(false, 8, 8 * MiB), "one-shot W=8 boundary\n");
-    CHECK(!auto_staged(false, 16, 4 * MiB - 16) && auto_staged(false, 16, 4 * MiB), "one-shot W=16 boundary\n");
-    CHECK(auto_staged(true, 2, 16) && auto_staged(true, 1, 16), "two-shot W<=2 not staged\n");
-    CHECK(!auto_staged(true, 4, 8 * MiB - 16) && auto_staged(true, 4, 8 * MiB) && auto_staged(true, 16, 8 * MiB),
+    CHECK(!auto_staged(false, 2, 64 * MiB, 1) && !auto_staged(false, 2, 1024 * MiB, 1), "one-shot W=2 staged\n");
+    CHECK(!auto_staged(false, 4, 16 * MiB - 16, 1) && auto_staged(false, 4, 16 * MiB, 1), "one-shot W=4 boundary\n");
+    CHECK(!auto_staged(false, 8, 8 * MiB - 16, 1) && auto_staged(false, 8, 8 * MiB, 1), "one-shot W=8 boundary\n");
+    CHECK(!auto_staged(false, 16, 4 * MiB - 16, 1) && auto_staged(false, 16, 4 * MiB, 1), "one-shot W=16 boundary\n");
+    CHECK(auto_staged(true, 2, 16, 2) && auto_staged(true, 1, 16, 1), "two-shot W<=2 not staged\n");
+    CHECK(!auto_staged(true, 4, 8 * MiB - 16, 4) && auto_staged(true, 4, 8 * MiB, 4) && auto_staged(true, 16, 8 * MiB, 16),
           "two-shot 8 MiB boundary\n");
-    CHECK(!auto_bulk_oneshot(8, 1024 * MiB) && !auto_bulk_oneshot(2, 1024 * MiB), "copy-off bulk one-shot at W<=8\n");
-    CHECK(!auto_bulk_oneshot(16, 8 * MiB - 16) && auto_bulk_oneshot(16, 8 * MiB) && auto_bulk_oneshot(9, 15 * MiB),
+    CHECK(!auto_bulk_oneshot(8, 1024 * MiB, 1) && !auto_bulk_oneshot(2, 1024 * MiB, 1), "copy-off bulk one-shot at W<=8\n");
+    CHECK(!auto_bulk_oneshot(16, 8 * MiB - 16, 1) && auto_bulk_oneshot(16, 8 * MiB, 1) && auto_bulk_oneshot(9, 15 * MiB, 1),
           "copy-off bulk one-shot boundary\n");
+    CHECK(auto_staged(false, 8, 32 * MiB, 2) && !auto_staged(false, 8, 32 * MiB, 3) &&
+              !auto_staged(false, 4, 32 * MiB, 2) && auto_staged(false, 16, 8 * MiB, 4) &&
+              !auto_staged(false, 16, 32 * MiB, 16), "one-shot staged with several outputs\n");
+    CHECK(auto_bulk_oneshot(16, 8 * MiB, 2) && auto_bulk_oneshot(16, 8 * MiB, 8) && !auto_bulk_oneshot(16, 8 * MiB, 9) &&
+              !auto_bulk_oneshot(16, 32 * MiB - 16, 16) && auto_bulk_oneshot(16, 32 * MiB, 16),
+          "copy-off bulk one-shot with several outputs\n");
     {
         GatherArgs g{};
         g.W = 8;

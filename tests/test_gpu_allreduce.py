@@ -514,3 +514,29 @@ def test_automatic_oneshot_engine_copy_off(rr, case):
     for r in (0, W - 1):
         assert_bitwise(outs.host(r), want, f"{case} output {r}")
     outs.check_guards()
+
+
+AUTO_ALL_OUTPUT_CASES = {
+    # (copy_mode, W, bf16 elements per rank, engine expected) for the one-shot with every output kept
+    "copy_W4_32MiB": (1, 4, 16 << 20, 1),
+    "copy_W8_8MiB": (1, 8, 4 << 20, 1),
+    "off_W16_8MiB": (0, 16, 4 << 20, 1),
+    "off_W16_32MiB": (0, 16, 16 << 20, 2),
+}
+
+
+@pytest.mark.parametrize("case", list(AUTO_ALL_OUTPUT_CASES))
+def test_automatic_oneshot_engine_all_outputs(rr, case):
+    """The one-shot's automatic engines count the kept outputs: with every
+    output kept the staged kernel gives way to the load/store one, and the
+    copy-off bulk-copy kernel needs 512 MiB read per output."""
+    copy, W, N, expect = AUTO_ALL_OUTPUT_CASES[case]
+    ins = workloads.rank_buffers(W, N, "bf16", "normal", seed_base=4500 + W)
+    want = oracle.allreduce(ins, "bf16")
+    pad = pad_for(rr, W)
+    pad.set_option("reduce_engine", 0)
+    _, _, outs = run_allreduce(rr, "oneshot", W, N, "bf16", copy, ins)
+    assert pad.get_option("last_engine") == expect
+    for r in (0, W // 2, W - 1):
+        assert_bitwise(outs.host(r), want, f"{case} output {r}")
+    outs.check_guards()
